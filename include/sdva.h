@@ -1,0 +1,186 @@
+/*
+ * sdva.h -- C ABI of the speculative-decoding verify step on one GB300 GPU.
+ *
+ * One speculative round of single-model LLM serving ends with a verify step:
+ * the main model takes the lane's window of 1 + d tokens (the last committed
+ * token followed by d drafted tokens), writes their K/V into the paged KV
+ * cache, runs one attention pass of the whole window over the cached context,
+ * and accepts the longest drafted prefix its own argmax agrees with.
+ * Sources: Baseten talk summary, section "추측 디코드" (drafts are checked
+ * by the main model in a single forward pass and the accepted ones are
+ * streamed); NInfer review (blog.123qwe.co.kr/?p=4624), section "아키텍처 ③"
+ * (MTP proposes 1..5 drafts, DFlash/DFlash2 1..15) and section "아키텍처 ①"
+ * (output stays provisional until the model accepts the commit).
+ *
+ * This library implements the three data-parallel calls of that step:
+ *   kv_append_quant  -- write new K/V rows into the quantised, paged cache
+ *   verify_attn      -- batched, causal-in-window, GQA attention of every
+ *                       lane's window over its whole cached context
+ *   spec_accept      -- argmax per window position, longest agreeing draft
+ *                       prefix, optional commit of the new lengths
+ *
+ * Conventions for every call
+ *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA
+ *     memory on the current device) unless stated otherwise; the caller owns
+ *     all memory.  The library allocates nothing, keeps no per-call state and
+ *     never synchronises: every call only enqueues kernels on `stream`
+ *     (NULL = the legacy default stream) and returns.
+ *   - Host-side argument errors are returned as negative codes (SDVA_ERR_*)
+ *     before anything is enqueued.  Errors that depend on device data (a bad
+ *     page id, a lane whose length does not fit, an out-of-vocabulary draft)
+ *     are reported by OR-ing SDVA_STATUS_* bits into the optional device int
+ *     `*status`; the affected lane is skipped as documented per call, never
+ *     trapped.  Read `*status` after the stream has completed.
+ *   - Launch shapes depend only on host arguments, so every call can be
+ *     captured in a CUDA graph and replayed.
+ *   - Inputs are not modified except where a parameter says "in/out".
+ *     Outputs must not alias inputs.
+ *
+ * KV cache layout (reading taken for the pages' "FP8 E4M3" KV and 4-bit KV;
+ * NInfer review section "성능과 평가", MegaCapybara announcement item 2):
+ *   page_size = 64 tokens, head_dim = 128, pages shared by all kv heads.
+ *   SDVA_KV_FP8_E4M3:
+ *     k_codes, v_codes : uint8  [num_pages][num_kv_heads][64][128]  OCP E4M3
+ *     k_scales, v_scales: float [num_pages][num_kv_heads]
+ *     value = e4m3(code) * scale.  The scale of a (page, head) only grows while
+ *     the page fills: an append starting at page offset 0 sets it to amax/448;
+ *     a later append into the same page raises it to max(old, amax/448) and,
+ *     if it grew, re-encodes the page's earlier tokens as
+ *     e4m3_rne_sat(fp32(e4m3(c) * s_old) / s_new).  New tokens are encoded as
+ *     e4m3_rne_sat(x / s) (fp32 IEEE division, round to nearest even,
+ *     saturating to +-448); a zero scale gives zero codes.
+ *   SDVA_KV_INT4_G32:
+ *     k_codes, v_codes : uint8  [num_pages][num_kv_heads][64][64]
+ *                        dim 2i in the low nibble, dim 2i+1 in the high
+ *                        nibble, two's complement, values in [-7, 7]
+ *     k_scales, v_scales: fp16 bits [num_pages][num_kv_heads][64][4]
+ *                        one scale per token and group of 32 head dims
+ *     s = fp16_rne(min(amax_group / 7, 65504)); code = clamp(rint(x / s), -7, 7)
+ *     with halves to even; value = code * s.
+ *   page_table: int32 [num_lanes][max_pages_per_lane]; entry p of lane b is
+ *     the physical page holding the lane's tokens [64p, 64p + 64).
+ *   seq_lens: int32 [num_lanes], L_b = tokens already cached for lane b
+ *     before the step (the same pre-step array is passed to all three calls;
+ *     spec_accept's commit is the last thing to change it).
+ */
+#ifndef SDVA_H
+#define SDVA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* sdva_stream_t;
+
+typedef enum { SDVA_KV_FP8_E4M3 = 0, SDVA_KV_INT4_G32 = 1 } sdva_kv_dtype;
+
+/* Description of a caller-owned cache; all four arrays are device memory
+ * laid out as above. */
+typedef struct {
+    int32_t dtype;        /* sdva_kv_dtype */
+    int32_t num_pages;    /* physical pages in the pool */
+    int32_t page_size;    /* must be 64 */
+    int32_t num_kv_heads; /* >= 1 */
+    int32_t head_dim;     /* must be 128 */
+    void* k_codes;
+    void* v_codes;
+    void* k_scales;
+    void* v_scales;
+} sdva_kv_cache;
+
+/* Host return codes. */
+#define SDVA_OK 0
+#define SDVA_ERR_INVALID (-1)     /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+#define SDVA_ERR_UNSUPPORTED (-2) /* head_dim != 128, page_size != 64, window > 16, dtype */
+#define SDVA_ERR_WORKSPACE (-3)   /* workspace missing or smaller than required */
+#define SDVA_ERR_CUDA (-4)        /* a kernel launch failed (cudaGetLastError) */
+
+/* Device status bits, OR-ed into *status. */
+#define SDVA_STATUS_BAD_PAGE 1  /* a needed page_table entry is outside [0, num_pages) */
+#define SDVA_STATUS_OVERFLOW 2  /* L_b < 0, or L_b + n does not fit the lane's row / max_context */
+#define SDVA_STATUS_BAD_DRAFT 4 /* a draft id is outside [0, vocab) */
+#define SDVA_STATUS_TIMEOUT 8   /* a bounded device wait gave up */
+
+/*
+ * kv_append_quant -- write tokens [L_b, L_b + n_new) of every lane into the
+ * cache (in/out), quantising as described above.
+ *   k_new, v_new : bf16 [num_lanes][n_new][num_kv_heads][128]
+ *   n_new        : >= 1; the verify window (1 + d) in a speculative step, or
+ *                  any chunk length when filling a context.
+ *   page_table, max_pages_per_lane, seq_lens: as above (seq_lens is read only).
+ *   status       : nullable device int.
+ * A lane with L_b < 0 or L_b + n_new > 64 * max_pages_per_lane gets
+ * SDVA_STATUS_OVERFLOW; a lane whose touched pages include an invalid id gets
+ * SDVA_STATUS_BAD_PAGE; in both cases nothing of that lane is written.
+ * Precondition: inputs are finite; no two lanes map the same physical page
+ * within one call; appends to a lane arrive in position order.
+ * Returns SDVA_OK or a negative SDVA_ERR_*.
+ */
+int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes, int n_new,
+                    const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens, int32_t* status,
+                    sdva_stream_t stream);
+
+/*
+ * verify_attn_workspace_size -- bytes of device scratch verify_attn needs for
+ * these sizes (split-K partial results).  Pure host function.  num_sms = 0
+ * queries the current device; pass the same arguments to verify_attn.
+ * Returns 0 for arguments verify_attn would reject.
+ */
+size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, int num_kv_heads, int max_context,
+                                  int num_sms);
+
+/*
+ * verify_attn -- for lane b, window position i in [0, window) and q head h:
+ *     out[b][i][h] = softmax_j(sm_scale * q . K_j) . V_j  over j in [0, L_b + i]
+ * with K_j, V_j the dequantised cache rows of kv head h / (Hq / Hkv): the
+ * cached context followed by the window's own tokens, which must already
+ * have been appended (causal inside the window).
+ *   q   : bf16 [num_lanes][window][num_q_heads][128]   (|q| < 65504)
+ *   out : bf16 [num_lanes][window][num_q_heads][128]   (written in full)
+ *   window: 1 .. 16.   max_context: host upper bound on every L_b.
+ *   workspace: device scratch of at least verify_attn_workspace_size(...) bytes,
+ *     256-byte aligned, used only during the call's kernels (its contents
+ *     between calls do not matter).
+ * A lane with L_b < 0, L_b > max_context or L_b + window > 64 *
+ * max_pages_per_lane gets SDVA_STATUS_OVERFLOW; a lane with an invalid page id
+ * among its first ceil((L_b + window) / 64) entries gets SDVA_STATUS_BAD_PAGE;
+ * the output rows of such a lane are set to zero.
+ * Returns SDVA_OK or a negative SDVA_ERR_*.
+ */
+int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens, int max_context,
+                float sm_scale, void* out, void* workspace, size_t workspace_bytes, int32_t* status,
+                sdva_stream_t stream);
+
+/*
+ * spec_accept -- greedy acceptance of a verify window.
+ *   logits    : fp32 [num_lanes][window][vocab]; row i scores the token that
+ *               follows window position i.
+ *   drafts    : int32 [num_lanes][window - 1]; drafts[b][i] is window token
+ *               i + 1 (nullable when window == 1).
+ *   out_tokens: int32 [num_lanes][window] (out): argmax of each row, ties to
+ *               the lowest index, NaN never wins, an all-NaN row gives 0.
+ *   accept_len: int32 [num_lanes] (out): a = number of leading i < window - 1
+ *               with drafts[b][i] == out_tokens[b][i].  The bonus token is
+ *               out_tokens[b][a].
+ *   seq_lens_inout: nullable int32 [num_lanes] (in/out): when given, the
+ *               commit adds 1 + a to each lane's length.
+ * An out-of-vocabulary draft id never matches and sets SDVA_STATUS_BAD_DRAFT.
+ * Returns SDVA_OK or a negative SDVA_ERR_*.
+ */
+int spec_accept(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
+                int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout, int32_t* status,
+                sdva_stream_t stream);
+
+/* Static description of a return code or status bit set (never NULL). */
+const char* sdva_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDVA_H */

@@ -1,0 +1,204 @@
+"""Python binding of libsdva, the GB300 verify-step library.
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of ``libsdva.so`` (built in-tree by ``build.py``).  There is no
+Python or CPU fallback; importing this package without the built library
+raises.  PyTorch supplies device memory and streams.
+
+The calls mirror ``include/sdva.h``:
+
+    kv_append_quant(cache, k_new, v_new, page_table, seq_lens, status=None, stream=None)
+    verify_attn_workspace_size(num_lanes, window, num_q_heads, num_kv_heads, max_context, num_sms=0)
+    verify_attn(cache, q, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None, stream=None)
+    spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
+    sdva_status_string(code)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsdva.so")
+
+KV_FP8_E4M3 = 0
+KV_INT4_G32 = 1
+PAGE = 64
+HEAD_DIM = 128
+MAX_WINDOW = 16
+
+OK = 0
+ERR_INVALID = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+STATUS_BAD_PAGE = 1
+STATUS_OVERFLOW = 2
+STATUS_BAD_DRAFT = 4
+STATUS_TIMEOUT = 8
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+        "or python speculative_decode_verify_append_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class _KVCacheStruct(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+    ]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_lib.kv_append_quant.restype = _I
+_lib.kv_append_quant.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _P, _I, _I, _P, _I, _P, _P, _P]
+_lib.verify_attn_workspace_size.restype = ctypes.c_size_t
+_lib.verify_attn_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+_lib.verify_attn.restype = _I
+_lib.verify_attn.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float, _P,
+                             _P, ctypes.c_size_t, _P, _P]
+_lib.spec_accept.restype = _I
+_lib.spec_accept.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+_lib.sdva_status_string.restype = ctypes.c_char_p
+_lib.sdva_status_string.argtypes = [_I]
+
+EXPORTED = ("kv_append_quant", "verify_attn_workspace_size", "verify_attn", "spec_accept", "sdva_status_string")
+
+
+class SdvaError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call}: {sdva_status_string(code)} (code {code})")
+        self.code = code
+
+
+def sdva_status_string(code: int) -> str:
+    return _lib.sdva_status_string(int(code)).decode()
+
+
+def _check(call: str, rc: int) -> None:
+    if rc != OK:
+        raise SdvaError(call, rc)
+
+
+def _dptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, name: str = "tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class KVCache:
+    """Caller-owned paged KV cache (device tensors in the library's layout).
+
+    FP8:  k_codes/v_codes uint8 [pages][Hkv][64][128]; k_scales/v_scales float32 [pages][Hkv]
+    INT4: k_codes/v_codes uint8 [pages][Hkv][64][64];  k_scales/v_scales float16 [pages][Hkv][64][4]
+    """
+
+    def __init__(self, dtype: int, num_pages: int, num_kv_heads: int, device="cuda", tensors=None):
+        self.dtype = int(dtype)
+        self.num_pages = int(num_pages)
+        self.num_kv_heads = int(num_kv_heads)
+        if tensors is not None:
+            self.k_codes, self.v_codes, self.k_scales, self.v_scales = tensors
+        elif self.dtype == KV_FP8_E4M3:
+            shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
+            self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+            self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+            self.k_scales = torch.zeros((num_pages, num_kv_heads), dtype=torch.float32, device=device)
+            self.v_scales = torch.zeros((num_pages, num_kv_heads), dtype=torch.float32, device=device)
+        elif self.dtype == KV_INT4_G32:
+            shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 2)
+            sshape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 32)
+            self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+            self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+            self.k_scales = torch.zeros(sshape, dtype=torch.float16, device=device)
+            self.v_scales = torch.zeros(sshape, dtype=torch.float16, device=device)
+        else:
+            raise ValueError(f"unknown kv dtype {dtype}")
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.k_codes, self.v_codes, self.k_scales, self.v_scales))
+
+    def struct(self) -> _KVCacheStruct:
+        return _KVCacheStruct(self.dtype, self.num_pages, PAGE, self.num_kv_heads, HEAD_DIM,
+                              _dptr(self.k_codes, name="k_codes"), _dptr(self.v_codes, name="v_codes"),
+                              _dptr(self.k_scales, name="k_scales"), _dptr(self.v_scales, name="v_scales"))
+
+
+def kv_append_quant(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, page_table: torch.Tensor,
+                    seq_lens: torch.Tensor, status: torch.Tensor | None = None, stream=None) -> None:
+    """k_new, v_new: bf16 [B][n_new][Hkv][128]; page_table int32 [B][max_pages]; seq_lens int32 [B]."""
+    B, n_new = k_new.shape[0], k_new.shape[1]
+    s = cache.struct()
+    rc = _lib.kv_append_quant(ctypes.byref(s), _dptr(k_new, torch.bfloat16, "k_new"),
+                              _dptr(v_new, torch.bfloat16, "v_new"), B, n_new,
+                              _dptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                              _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(status, torch.int32, "status"),
+                              _stream(stream))
+    _check("kv_append_quant", rc)
+
+
+def verify_attn_workspace_size(num_lanes: int, window: int, num_q_heads: int, num_kv_heads: int, max_context: int,
+                               num_sms: int = 0) -> int:
+    return int(_lib.verify_attn_workspace_size(num_lanes, window, num_q_heads, num_kv_heads, max_context, num_sms))
+
+
+def verify_attn(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                max_context: int, sm_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                status: torch.Tensor | None = None, stream=None) -> None:
+    """q, out: bf16 [B][W][Hq][128]; workspace: uint8 device tensor of at least
+    verify_attn_workspace_size(...) bytes."""
+    B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+    s = cache.struct()
+    rc = _lib.verify_attn(ctypes.byref(s), _dptr(q, torch.bfloat16, "q"), Hq, B, W,
+                          _dptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                          _dptr(seq_lens, torch.int32, "seq_lens"), int(max_context), float(sm_scale),
+                          _dptr(out, torch.bfloat16, "out"), _dptr(workspace, None, "workspace"),
+                          workspace.numel() * workspace.element_size(), _dptr(status, torch.int32, "status"),
+                          _stream(stream))
+    _check("verify_attn", rc)
+
+
+def spec_accept(logits: torch.Tensor, drafts: torch.Tensor | None, accept_len: torch.Tensor,
+                out_tokens: torch.Tensor, seq_lens_inout: torch.Tensor | None = None,
+                status: torch.Tensor | None = None, stream=None) -> None:
+    """logits fp32 [B][W][V]; drafts int32 [B][W-1]; accept_len int32 [B]; out_tokens int32 [B][W]."""
+    B, W, V = logits.shape
+    rc = _lib.spec_accept(_dptr(logits, torch.float32, "logits"), B, W, V,
+                          _dptr(drafts, torch.int32, "drafts") if W > 1 else None,
+                          _dptr(accept_len, torch.int32, "accept_len"), _dptr(out_tokens, torch.int32, "out_tokens"),
+                          _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"), _dptr(status, torch.int32, "status"),
+                          _stream(stream))
+    _check("spec_accept", rc)
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded C library (for callers that pass raw pointers themselves)."""
+    return _lib

@@ -1,0 +1,235 @@
+// kv_append.cu -- kv_append_quant: write the verify window's new K/V rows into
+// the paged, quantised KV cache.
+//
+// FP8 E4M3 cache with one fp32 scale per (page, kv head): the KV format the
+// NInfer review names in section "성능과 평가" ("FP8 E4M3" KV).  INT4 cache with
+// an fp16 scale per token and group of 32 head dims: the 4-bit KV setting of
+// the MegaCapybara announcement, item 2.  The scale rules (a page's FP8 scale
+// only grows while it fills; growth re-encodes the page's earlier tokens) are
+// the reading this library takes; they are spelled out in sdva.h.
+//
+// Both kernels are launch-bound (a verify window is at most 16 tokens, 64 KB
+// of bf16 input at 12 lanes): one CTA per (touched page, lane[, kv head, K|V]),
+// 16-byte vector loads and stores, fp32 arithmetic through explicitly rounded
+// intrinsics (__fdiv_rn / __fmul_rn) so that no contraction or approximate
+// division can change a code.
+#include "sdva_common.cuh"
+
+namespace sdva {
+namespace {
+
+struct AppendArgs {
+  const uint16_t* k_new;  // bf16 [B][n_new][Hkv][128]
+  const uint16_t* v_new;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  void* k_scales;
+  void* v_scales;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t* status;
+  int num_pages, num_kv_heads, n_new, max_pages;
+};
+
+constexpr int kAppendThreads = 256;
+
+// Lane admission shared by both kernels: the whole token range must fit the
+// lane's page-table row and every touched page id must be valid; otherwise
+// the lane is skipped and flagged (once, by the lane's first CTA).
+__device__ bool lane_admitted(const AppendArgs& a, int b, int L, bool report) {
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const long long end = (long long)L + a.n_new;
+  if (L < 0 || end > (long long)a.max_pages * kPage) {
+    if (report && threadIdx.x == 0) raise_status(a.status, SDVA_STATUS_OVERFLOW);
+    return false;
+  }
+  const int32_t* row = a.page_table + (size_t)b * a.max_pages;
+  const int first = L / kPage, last = (int)((end - 1) / kPage);
+  for (int p = first + (int)threadIdx.x; p <= last; p += blockDim.x) {
+    const int id = row[p];
+    if (id < 0 || id >= a.num_pages) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (report && threadIdx.x == 0) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float block_max(float v) {
+  __shared__ float s_part[kAppendThreads / 32];
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = s_part[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, s_part[w]);
+  return r;
+}
+
+// grid: (touched-page slot, lane, kv_head * 2 + {0: K, 1: V})
+__global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a) {
+  const int slot = blockIdx.x, b = blockIdx.y;
+  const int hk = blockIdx.z >> 1, is_v = blockIdx.z & 1;
+  const int L = a.seq_lens[b];
+  if (!lane_admitted(a, b, L, slot == 0 && blockIdx.z == 0)) return;
+  const int lp = L / kPage + slot;
+  if ((long long)lp * kPage >= (long long)L + a.n_new) return;
+  const int pid = a.page_table[(size_t)b * a.max_pages + lp];
+  const int t0 = max(L, lp * kPage), t1 = min(L + a.n_new, lp * kPage + kPage);
+  const int start = t0 - lp * kPage, count = t1 - t0;
+  const size_t token_stride = (size_t)a.num_kv_heads * kHeadDim;
+  const uint16_t* src = (is_v ? a.v_new : a.k_new) + ((size_t)b * a.n_new + (t0 - L)) * token_stride +
+                        (size_t)hk * kHeadDim;
+  uint8_t* codes = (is_v ? a.v_codes : a.k_codes) + ((size_t)pid * a.num_kv_heads + hk) * kPage * kHeadDim;
+  float* scale = reinterpret_cast<float*>(is_v ? a.v_scales : a.k_scales) + (size_t)pid * a.num_kv_heads + hk;
+
+  // items: (token, 8 consecutive dims) -> one 16-byte load each, <= 4 per thread
+  constexpr int kMaxItems = kPage * kHeadDim / 8 / kAppendThreads;
+  uint4 x[kMaxItems];
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kMaxItems; ++k) {
+    const int it = threadIdx.x + k * kAppendThreads;
+    if (it < count * (kHeadDim / 8)) {
+      const int t = it >> 4, g = it & 15;
+      x[k] = *reinterpret_cast<const uint4*>(src + (size_t)t * token_stride + g * 8);
+      const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    }
+  }
+  amax = block_max(amax);
+  const float s_old = *scale;  // read by every thread before the barrier below
+  const float s_cand = __fdiv_rn(amax, 448.0f);
+  const float s_new = (start == 0) ? s_cand : (s_cand > s_old ? s_cand : s_old);
+
+  if (start > 0 && s_new > s_old) {
+    // earlier tokens of the page move to the larger scale: 4 codes per item
+    uint32_t* old = reinterpret_cast<uint32_t*>(codes);
+    for (int it = threadIdx.x; it < start * (kHeadDim / 4); it += blockDim.x) {
+      const uint32_t c = old[it];
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fdiv_rn(__fmul_rn(e4m3_to_f32((c >> (8 * j)) & 0xFFu), s_old), s_new);
+      old[it] = (uint32_t)e4m3x2_from_f32(v[0], v[1]) | ((uint32_t)e4m3x2_from_f32(v[2], v[3]) << 16);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxItems; ++k) {
+    const int it = threadIdx.x + k * kAppendThreads;
+    if (it < count * (kHeadDim / 8)) {
+      const int t = it >> 4, g = it & 15;
+      uint2 out = make_uint2(0u, 0u);
+      if (s_new != 0.0f) {
+        const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+        uint32_t p[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          p[j] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[j]), s_new), __fdiv_rn(bf16_hi(w[j]), s_new));
+        out.x = p[0] | (p[1] << 16);
+        out.y = p[2] | (p[3] << 16);
+      }
+      *reinterpret_cast<uint2*>(codes + (size_t)(start + t) * kHeadDim + g * 8) = out;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *scale = s_new;
+}
+
+// grid: (touched-page slot, lane).  One thread per (token, kv head, K|V,
+// group of 32 dims): 64 bytes in, 16 bytes of codes and one fp16 scale out.
+__global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs a) {
+  const int slot = blockIdx.x, b = blockIdx.y;
+  const int L = a.seq_lens[b];
+  if (!lane_admitted(a, b, L, slot == 0)) return;
+  const int lp = L / kPage + slot;
+  if ((long long)lp * kPage >= (long long)L + a.n_new) return;
+  const int pid = a.page_table[(size_t)b * a.max_pages + lp];
+  const int t0 = max(L, lp * kPage), t1 = min(L + a.n_new, lp * kPage + kPage);
+  const int count = t1 - t0;
+  const int H = a.num_kv_heads;
+  const size_t token_stride = (size_t)H * kHeadDim;
+  for (int it = threadIdx.x; it < count * H * 8; it += blockDim.x) {
+    const int g = it & 3, is_v = (it >> 2) & 1, rest = it >> 3;
+    const int hk = rest % H, t = rest / H;
+    const int off = t0 + t - lp * kPage;
+    const uint16_t* src = (is_v ? a.v_new : a.k_new) + ((size_t)b * a.n_new + (t0 - L + t)) * token_stride +
+                          (size_t)hk * kHeadDim + g * 32;
+    float x[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(src)[q];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[q * 8 + 2 * j] = bf16_lo(w[j]);
+        x[q * 8 + 2 * j + 1] = bf16_hi(w[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    const __half s16 = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
+    const float sf = __half2float(s16);
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if (sf != 0.0f) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        int qv = __float2int_rn(__fdiv_rn(x[j], sf));
+        qv = max(-7, min(7, qv));
+        packed[j >> 3] |= (uint32_t)(qv & 0xF) << (4 * (j & 7));
+      }
+    }
+    const size_t ph = (size_t)pid * H + hk;
+    uint8_t* codes = (is_v ? a.v_codes : a.k_codes) + (ph * kPage + off) * (kHeadDim / 2) + g * 16;
+    *reinterpret_cast<uint4*>(codes) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    __half* scales = reinterpret_cast<__half*>(is_v ? a.v_scales : a.k_scales);
+    scales[(ph * kPage + off) * (kHeadDim / 32) + g] = s16;
+  }
+}
+
+}  // namespace
+}  // namespace sdva
+
+using namespace sdva;
+
+extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes,
+                               int n_new, const int32_t* page_table, int max_pages_per_lane,
+                               const int32_t* seq_lens, int32_t* status, sdva_stream_t stream) {
+  if (cache == nullptr || k_new == nullptr || v_new == nullptr || page_table == nullptr || seq_lens == nullptr)
+    return SDVA_ERR_INVALID;
+  if (cache->k_codes == nullptr || cache->v_codes == nullptr || cache->k_scales == nullptr ||
+      cache->v_scales == nullptr)
+    return SDVA_ERR_INVALID;
+  if (num_lanes <= 0 || n_new <= 0 || max_pages_per_lane <= 0 || cache->num_pages <= 0 ||
+      cache->num_kv_heads <= 0)
+    return SDVA_ERR_INVALID;
+  if (cache->page_size != kPage || cache->head_dim != kHeadDim) return SDVA_ERR_UNSUPPORTED;
+  if (cache->dtype != SDVA_KV_FP8_E4M3 && cache->dtype != SDVA_KV_INT4_G32) return SDVA_ERR_UNSUPPORTED;
+  if (num_lanes > 65535 || cache->num_kv_heads > 32767) return SDVA_ERR_UNSUPPORTED;
+  AppendArgs a;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_codes = static_cast<uint8_t*>(cache->k_codes);
+  a.v_codes = static_cast<uint8_t*>(cache->v_codes);
+  a.k_scales = cache->k_scales;
+  a.v_scales = cache->v_scales;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.status = status;
+  a.num_pages = cache->num_pages;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.n_new = n_new;
+  a.max_pages = max_pages_per_lane;
+  const int slots = (n_new + kPage - 1) / kPage + 1;  // pages a range of n_new tokens can touch
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cache->dtype == SDVA_KV_FP8_E4M3) {
+    append_fp8_kernel<<<dim3(slots, num_lanes, cache->num_kv_heads * 2), kAppendThreads, 0, s>>>(a);
+  } else {
+    append_int4_kernel<<<dim3(slots, num_lanes), kAppendThreads, 0, s>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
+}

@@ -1,0 +1,116 @@
+"""The C ABI (no GPU): libsdva.so builds for sm_103a, loads, exports every
+function include/sdva.h declares, and its pure-host logic (workspace sizing,
+status strings, argument validation that returns before any CUDA call)
+behaves as the header documents."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._load_builder().build()
+    return ctypes.CDLL(path)
+
+
+def _declared_functions():
+    names = []
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            name = m.group(1)
+            if name not in ("if", "while", "sizeof", "defined"):
+                names.append(name)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = _declared_functions()
+    for n in ("kv_append_quant", "verify_attn", "spec_accept", "verify_attn_workspace_size", "sdva_status_string"):
+        assert n in names, names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    path = lib._name
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in _declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+
+
+def test_library_targets_sm103a(lib):
+    out = subprocess.run(["cuobjdump", "--list-elf", lib._name], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_workspace_size_host_logic(lib):
+    f = lib.verify_attn_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 6
+    a = f(8, 16, 24, 4, 65536, 152)
+    b = f(8, 16, 24, 4, 131072, 152)
+    assert a > 0 and b >= a
+    assert f(1, 1, 24, 4, 32768, 152) > 0
+    assert f(1, 17, 24, 4, 1000, 152) == 0     # window > 16
+    assert f(1, 4, 25, 4, 1000, 152) == 0      # Hq % Hkv != 0
+    assert f(0, 4, 24, 4, 1000, 152) == 0
+    # partials: (m, l) + 128 fp32 per row per split, 256-byte aligned sections
+    assert a % 4 == 0
+
+
+def test_status_strings(lib):
+    f = lib.sdva_status_string
+    f.restype = ctypes.c_char_p
+    f.argtypes = [ctypes.c_int]
+    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 3, -99):
+        s = f(code)
+        assert s and len(s) >= 2
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("k_codes", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p)]
+
+
+def test_argument_validation_returns_before_cuda(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    c = _Cache(0, 4, 64, 1, 128, fake, fake, fake, fake)
+    app = lib.kv_append_quant
+    app.restype = ctypes.c_int
+    assert app(ctypes.byref(c), None, fake, 1, 1, fake, 1, fake, None, None) == -1
+    assert app(ctypes.byref(c), fake, fake, 1, 0, fake, 1, fake, None, None) == -1
+    c.head_dim = 64
+    assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
+    c.head_dim, c.page_size = 128, 32
+    assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
+    c.page_size, c.dtype = 64, 7
+    assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
+    c.dtype = 0
+    va = lib.verify_attn
+    va.restype = ctypes.c_int
+    va.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_float,
+                   P, P, ctypes.c_size_t, P, P]
+    assert va(ctypes.byref(c), fake, 4, 1, 17, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -2
+    c.num_kv_heads = 2
+    assert va(ctypes.byref(c), fake, 3, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
+    c.num_kv_heads = 1
+    assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, -1.0, fake, fake, 1 << 20, None, None) == -1
+    assert va(ctypes.byref(c), None, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
+    sa = lib.spec_accept
+    sa.restype = ctypes.c_int
+    assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
+    assert sa(fake, 0, 4, 100, fake, fake, fake, None, None, None) == -1

@@ -1,0 +1,115 @@
+"""The three calls together, as a serving loop issues them: several verify
+steps with commits (append -> verify_attn -> spec_accept), checked against
+the oracle replaying the same steps; CUDA-graph replay of a step; and
+checkpoint / restore of the caller-owned state."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import SM_SCALE, assert_close, bf16_dev, fill_both, i32_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _sdva():
+    import speculative_decode_verify_append_gb300 as sdva
+    from speculative_decode_verify_append_gb300.step import VerifyStep
+    return sdva, VerifyStep
+
+
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+def test_multi_step_loop_matches_oracle(dtype):
+    sdva, VerifyStep = _sdva()
+    W, Hq, Hkv, V = 6, 12, 2, 3000
+    lens = np.array([100, 640, 1333], np.int32)
+    steps = 5
+    spec = synth.Spec("loop", 11, 3, 0, 0, Hq, Hkv, W, dtype, V, 0.7, True)
+    # capacity for all steps
+    table, total = synth.page_table_for(spec, lens + steps * W, W)
+    step0 = synth.make_step(spec, seq_lens=lens, with_accept=False)
+    step0.page_table, step0.num_pages = table, total
+    gcache, ocache, st = fill_both(spec, step0, chunk=256)  # includes step 0's window append
+    vs = VerifyStep(3, W, Hq, Hkv, int(lens.max()) + steps * W, V)
+    L_host = lens.copy()
+    L_dev = i32_dev(lens)
+    tdev = i32_dev(table)
+    for s in range(steps):
+        stp = synth.make_step(spec, seq_lens=L_host, tag=f"s{s}")
+        if s > 0:  # step 0's window is already appended by fill_both
+            vs.append(gcache, bf16_dev(stp.k_win), bf16_dev(stp.v_win), tdev, L_dev)
+            assert oracle.append(ocache, stp.k_win, stp.v_win, table, L_host) == 0
+        vs.attend(gcache, bf16_dev(stp.q), tdev, L_dev)
+        vs.accept(torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts), L_dev)
+        torch.cuda.synchronize()
+        want, _ = oracle.verify_attn(ocache, stp.q, table, L_host, SM_SCALE, threads=8)
+        assert_close(vs.out.float().cpu().numpy(), want, f"step {s}")
+        acc, tok, newL, _ = oracle.spec_accept(stp.logits, stp.drafts, L_host)
+        assert np.array_equal(vs.accept_len.cpu().numpy(), acc)
+        assert np.array_equal(vs.out_tokens.cpu().numpy(), tok)
+        assert np.array_equal(L_dev.cpu().numpy(), newL)
+        L_host = newL
+    assert int(vs.status.item()) == 0
+    g = {n: getattr(gcache, n).cpu().numpy() for n in ("k_codes", "v_codes")}
+    assert np.array_equal(g["k_codes"], ocache.k_codes) and np.array_equal(g["v_codes"], ocache.v_codes)
+
+
+def test_cuda_graph_replay_matches_eager():
+    sdva, VerifyStep = _sdva()
+    spec = synth.WORKLOADS["multi_lane"]
+    lens = np.array([4096, 700, 9000, 64], np.int32)
+    spec = synth.Spec("g", 3, 4, 0, 0, 24, 4, 16, synth.KV_FP8, 151936, 0.7, True)
+    stp = synth.make_step(spec, seq_lens=lens)
+    gcache, _, _ = fill_both(spec, stp, with_oracle=False)
+    vs = VerifyStep(4, 16, 24, 4, 9000, 151936)
+    q, t, L = bf16_dev(stp.q), i32_dev(stp.page_table), i32_dev(lens)
+    lg, dr = torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts)
+    kw, vw = bf16_dev(stp.k_win), bf16_dev(stp.v_win)
+    vs.run(gcache, q, kw, vw, t, L, lg, dr, commit=False)
+    torch.cuda.synchronize()
+    eager = (vs.out.clone(), vs.accept_len.clone(), vs.out_tokens.clone())
+    vs.out.zero_()
+    vs.accept_len.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            vs.run(gcache, q, kw, vw, t, L, lg, dr, commit=False, stream=s)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(vs.out, eager[0])
+    assert torch.equal(vs.accept_len, eager[1]) and torch.equal(vs.out_tokens, eager[2])
+
+
+def test_checkpoint_restore_continues_identically():
+    sdva, VerifyStep = _sdva()
+    W = 4
+    lens = np.array([500, 90], np.int32)
+    spec = synth.Spec("ck", 21, 2, 0, 0, 8, 2, W, synth.KV_FP8, 500, 0.7, True)
+    table, total = synth.page_table_for(spec, lens + 3 * W, W)
+    s0 = synth.make_step(spec, seq_lens=lens, with_accept=False)
+    s0.page_table, s0.num_pages = table, total
+    gcache, _, _ = fill_both(spec, s0, with_oracle=False)
+    vs = VerifyStep(2, W, 8, 2, 600, 500)
+    tdev = i32_dev(table)
+    L = i32_dev(lens)
+
+    def one_step(tag):
+        L_host = L.cpu().numpy()
+        stp = synth.make_step(spec, seq_lens=L_host, tag=tag)
+        vs.run(gcache, bf16_dev(stp.q), bf16_dev(stp.k_win), bf16_dev(stp.v_win), tdev, L,
+               torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts))
+        torch.cuda.synchronize()
+        return vs.out.clone(), vs.accept_len.clone()
+
+    one_step("a")
+    saved = [x.clone() for x in (gcache.k_codes, gcache.v_codes, gcache.k_scales, gcache.v_scales, L)]
+    first = [one_step("b"), one_step("c")]
+    for dst, src in zip((gcache.k_codes, gcache.v_codes, gcache.k_scales, gcache.v_scales, L), saved):
+        dst.copy_(src)
+    second = [one_step("b"), one_step("c")]
+    for (o1, a1), (o2, a2) in zip(first, second):
+        assert torch.equal(o1, o2) and torch.equal(a1, a2)

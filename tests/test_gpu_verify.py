@@ -1,0 +1,148 @@
+"""GPU parity of verify_attn against the oracle (fp64): every output element
+within |g - r| <= 2e-3 + 1e-2 |r| on small cases spanning several pages,
+splits and ragged tails, FP8 and INT4, and on sampled rows of the five
+full-size workloads in the benchmark's launch configuration; plus GPU-side
+invariants (page-table permutation, split count, invalid lanes)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import SM_SCALE, assert_close, bf16_dev, fill_both, i32_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _sdva():
+    import speculative_decode_verify_append_gb300 as sdva
+    return sdva
+
+
+def _run_verify(spec, step, gcache, max_context=None, table=None):
+    sdva = _sdva()
+    B, W, Hq = step.q.shape[:3]
+    max_context = int(step.seq_lens.max()) if max_context is None else max_context
+    table = step.page_table if table is None else table
+    out = torch.full((B, W, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sdva.verify_attn_workspace_size(B, W, Hq, spec.num_kv_heads, max_context), dtype=torch.uint8,
+                     device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sdva.verify_attn(gcache, bf16_dev(step.q), i32_dev(table), i32_dev(step.seq_lens), max_context, float(SM_SCALE),
+                     out, ws, status)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), int(status.item())
+
+
+SMALL = [
+    # (kv dtype, lens, W, Hq, Hkv)
+    (synth.KV_FP8, [0, 1, 63, 64, 65, 700], 1, 4, 1),
+    (synth.KV_FP8, [5, 200, 1500], 4, 24, 4),
+    (synth.KV_FP8, [130, 4097, 31], 16, 24, 4),
+    (synth.KV_FP8, [333, 64], 16, 8, 1),      # R = 128: one full CTA of rows
+    (synth.KV_FP8, [250, 20], 16, 16, 1),     # R = 256: two row blocks
+    (synth.KV_FP8, [2000], 6, 24, 4),
+    (synth.KV_INT4, [0, 64, 129, 900], 8, 24, 4),
+    (synth.KV_INT4, [1200, 77], 16, 12, 2),
+    (synth.KV_INT4, [700], 1, 4, 1),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{'fp8' if c[0] == 0 else 'int4'}-W{c[2]}-{c[3]}q{c[4]}kv")
+def test_small_cases_all_elements(case):
+    dtype, lens, W, Hq, Hkv = case
+    spec = synth.Spec("small", 17 + W, len(lens), 0, 0, Hq, Hkv, W, dtype, None, 0.7, True)
+    step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
+    gcache, ocache, st = fill_both(spec, step, chunk=512)
+    got, status = _run_verify(spec, step, gcache)
+    assert status == 0
+    want, ost = oracle.verify_attn(ocache, step.q, step.page_table, step.seq_lens, SM_SCALE, threads=8)
+    assert ost == 0
+    assert_close(got, want, str(case))
+
+
+@pytest.mark.parametrize("name", ["tiny", "plain_decode", "multi_lane", "long_context", "int4_12slot"])
+def test_full_workload_sampled_rows(name):
+    spec = synth.WORKLOADS[name]
+    step = synth.make_step(spec, with_accept=False)
+    B, W, Hq = step.q.shape[:3]
+    rng = np.random.default_rng(5)
+    # the oracle replays the fill of at most two lanes (every lane is on the GPU)
+    lanes = sorted(rng.choice(B, size=min(B, 2), replace=False).tolist())
+    gcache, ocache, st = fill_both(spec, step, lanes=lanes)
+    got, status = _run_verify(spec, step, gcache, max_context=spec.ctx_hi)
+    assert status == 0
+    assert np.isfinite(got).all()
+    rows = []
+    for b in lanes:
+        for i in sorted({0, W - 1, int(rng.integers(0, W))}):
+            for h in sorted({0, Hq - 1, int(rng.integers(0, Hq))}):
+                rows.append((b, i, h))
+    want, ost = oracle.verify_attn(ocache, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=rows, threads=16)
+    assert ost == 0
+    gsel = np.stack([got[b, i, h] for (b, i, h) in rows])
+    assert_close(gsel, want, name)
+
+
+def test_permuted_table_is_bit_identical():
+    lens, W = [900, 3000], 16
+    s1 = synth.Spec("p", 3, 2, 0, 0, 24, 4, W, synth.KV_FP8, None, 0.7, False)
+    s2 = synth.Spec("p", 3, 2, 0, 0, 24, 4, W, synth.KV_FP8, None, 0.7, True)
+    st1 = synth.make_step(s1, seq_lens=np.array(lens, np.int32), with_accept=False)
+    st2 = synth.make_step(s2, seq_lens=np.array(lens, np.int32), with_accept=False)
+    g1, _, _ = fill_both(s1, st1, with_oracle=False)
+    g2, _, _ = fill_both(s2, st2, with_oracle=False)
+    o1, _ = _run_verify(s1, st1, g1)
+    o2, _ = _run_verify(s2, st2, g2)
+    assert np.array_equal(o1, o2)
+
+
+def test_split_count_changes_only_rounding():
+    lens, W = [5000, 700], 8
+    spec = synth.Spec("s", 4, 2, 0, 0, 24, 4, W, synth.KV_FP8, None, 0.7, True)
+    step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
+    g, o, _ = fill_both(spec, step)
+    a, _ = _run_verify(spec, step, g, max_context=5000)
+    b, _ = _run_verify(spec, step, g, max_context=200000)  # far larger bound: different split plan
+    want, _ = oracle.verify_attn(o, step.q, step.page_table, step.seq_lens, SM_SCALE, threads=8)
+    assert_close(a, want)
+    assert_close(b, want)
+    assert np.abs(a - b).max() <= 2 * 2.0 ** -8 * np.abs(want).max()
+
+
+def test_invalid_lanes_are_zero_and_flagged():
+    sdva = _sdva()
+    lens, W = [300, 300, 300], 4
+    spec = synth.Spec("e", 6, 3, 0, 0, 8, 2, W, synth.KV_FP8, None, 0.7, True)
+    step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
+    g, _, _ = fill_both(spec, step, with_oracle=False)
+    table = step.page_table.copy()
+    table[1, 2] = step.num_pages + 3
+    got, status = _run_verify(spec, step, g, table=table)
+    assert status == sdva.STATUS_BAD_PAGE
+    assert not got[1].any() and np.isfinite(got).all() and got[0].any() and got[2].any()
+    step.seq_lens[2] = 10 ** 6
+    got, status = _run_verify(spec, step, g, max_context=300)
+    assert status & sdva.STATUS_OVERFLOW
+    assert not got[2].any()
+
+
+def test_host_argument_errors():
+    sdva = _sdva()
+    g = sdva.KVCache(synth.KV_FP8, 2, 1)
+    q = torch.zeros((1, 17, 4, 128), dtype=torch.bfloat16, device="cuda")
+    t = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    L = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sdva.SdvaError) as e:
+        sdva.verify_attn(g, q, t, L, 64, 0.088, q, ws)
+    assert e.value.code == sdva.ERR_UNSUPPORTED
+    q = q[:, :4].contiguous()
+    with pytest.raises(sdva.SdvaError) as e:
+        sdva.verify_attn(g, q, t, L, 64, 0.088, q.clone(), ws[:16])
+    assert e.value.code == sdva.ERR_WORKSPACE
+    q3 = torch.zeros((1, 4, 3, 128), dtype=torch.bfloat16, device="cuda")
+    g2 = sdva.KVCache(synth.KV_FP8, 2, 2)
+    with pytest.raises(sdva.SdvaError) as e:
+        sdva.verify_attn(g2, q3, t, L, 64, 0.088, q3.clone(), ws)
+    assert e.value.code == sdva.ERR_INVALID
