@@ -156,6 +156,37 @@ int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int 
                 float sm_scale, void* out, void* workspace, size_t workspace_bytes, int32_t* status,
                 sdva_stream_t stream);
 
+/* Bytes of the fixed device scratch behind verify_attn_noalloc (32 MiB). */
+#define SDVA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * verify_attn_noalloc -- verify_attn without a workspace argument, for callers
+ * that cannot allocate device memory at call time: runtimes that plan all of
+ * their device memory once at start-up and keep no headroom for per-call
+ * scratch, plugin hosts that give an operator only its own input and output
+ * tensors, and latency-critical loops that cannot pay for an allocator's
+ * implicit device synchronisation.  (The pages describe no such call; it is
+ * an addition of this library.)
+ *   Arguments, outputs, status bits and return codes are those of verify_attn.
+ *   The split-K scratch is a fixed, 256-byte-aligned array of
+ *   SDVA_NOALLOC_SCRATCH_BYTES compiled into this library's device image; every
+ *   GPU that loads the library holds it until the process exits.  The call
+ *   itself allocates nothing (no cudaMalloc / cudaFree).
+ *   Sizes whose verify_attn_workspace_size(...) exceeds
+ *   SDVA_NOALLOC_SCRATCH_BYTES are rejected with SDVA_ERR_WORKSPACE before
+ *   anything is enqueued.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ *   All calls share the one array and it keeps the last call's contents
+ *   (nothing in it needs to start at zero): calls whose kernels overlap on the
+ *   GPU -- on different streams, or from different threads -- race on it and
+ *   must be serialised by the caller.
+ */
+int verify_attn_noalloc(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                        const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
+                        int max_context, float sm_scale, void* out, int32_t* status, sdva_stream_t stream);
+
 /*
  * spec_accept -- greedy acceptance of a verify window.
  *   logits    : fp32 [num_lanes][window][vocab]; row i scores the token that

@@ -70,12 +70,17 @@ _lib.verify_attn_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
 _lib.verify_attn.restype = _I
 _lib.verify_attn.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float, _P,
                              _P, ctypes.c_size_t, _P, _P]
+_lib.verify_attn_noalloc.restype = _I
+_lib.verify_attn_noalloc.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float,
+                                     _P, _P, _P]
 _lib.spec_accept.restype = _I
 _lib.spec_accept.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
-EXPORTED = ("kv_append_quant", "verify_attn_workspace_size", "verify_attn", "spec_accept", "sdva_status_string")
+EXPORTED = ("kv_append_quant", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
+            "sdva_status_string")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class SdvaError(RuntimeError):
@@ -184,6 +189,21 @@ def verify_attn(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_l
                           workspace.numel() * workspace.element_size(), _dptr(status, torch.int32, "status"),
                           _stream(stream))
     _check("verify_attn", rc)
+
+
+def verify_attn_noalloc(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                        max_context: int, sm_scale: float, out: torch.Tensor, status: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """verify_attn with the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+    s = cache.struct()
+    rc = _lib.verify_attn_noalloc(ctypes.byref(s), _dptr(q, torch.bfloat16, "q"), Hq, B, W,
+                                  _dptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                                  _dptr(seq_lens, torch.int32, "seq_lens"), int(max_context), float(sm_scale),
+                                  _dptr(out, torch.bfloat16, "out"), _dptr(status, torch.int32, "status"),
+                                  _stream(stream))
+    _check("verify_attn_noalloc", rc)
 
 
 def spec_accept(logits: torch.Tensor, drafts: torch.Tensor | None, accept_len: torch.Tensor,

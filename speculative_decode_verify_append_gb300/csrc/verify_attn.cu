@@ -530,3 +530,64 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   verify_merge_kernel<<<plan.units, 256, 0, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// verify_attn_noalloc: the same verify_attn launches, with the split-K scratch
+// taken from a fixed array that is part of this library's device image instead
+// of a caller-provided workspace.  For callers that cannot allocate device
+// memory at call time: runtimes that plan every byte of device memory once at
+// start-up (a fixed pool with nothing left for per-call scratch), plugin hosts
+// that hand an operator only its own input and output tensors, and
+// latency-critical loops that must not pay for an allocator's implicit device
+// synchronisation.  The array is 256-byte aligned, holds
+// SDVA_NOALLOC_SCRATCH_BYTES, and lives on every GPU that loads the library
+// until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace sdva {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SDVA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxScratchDevices = 256;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxScratchDevices] = {};  // device address of the array, per device
+
+// Host code must not pass the array's name to a kernel: on the host it is a
+// stand-in symbol, not a device address.  The address is looked up once per
+// device, with that device current, and cached.
+int noalloc_scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDVA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxScratchDevices) return SDVA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> guard(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SDVA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SDVA_OK;
+}
+
+}  // namespace
+}  // namespace sdva
+
+extern "C" int verify_attn_noalloc(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
+                                   int window, const int32_t* page_table, int max_pages_per_lane,
+                                   const int32_t* seq_lens, int max_context, float sm_scale, void* out,
+                                   int32_t* status, sdva_stream_t stream) {
+  if (cache == nullptr || cache->num_kv_heads <= 0) return SDVA_ERR_INVALID;
+  // reject sizes beyond the fixed scratch before touching the device
+  const size_t need = verify_attn_workspace_size(num_lanes, window, num_q_heads, cache->num_kv_heads, max_context,
+                                                 sdva::device_sm_count());
+  if (need > SDVA_NOALLOC_SCRATCH_BYTES) return SDVA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = sdva::noalloc_scratch_for_current_device(&scratch);
+  if (rc != SDVA_OK) return rc;
+  // Nothing in the scratch needs to start at zero: every partial the merge
+  // reads is written earlier in the same call.
+  return verify_attn(cache, q, num_q_heads, num_lanes, window, page_table, max_pages_per_lane, seq_lens,
+                     max_context, sm_scale, out, scratch, SDVA_NOALLOC_SCRATCH_BYTES, status, stream);
+}
