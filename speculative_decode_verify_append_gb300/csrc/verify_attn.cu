@@ -25,6 +25,7 @@
 #include <math.h>
 
 #include "sdva_common.cuh"
+#include "verify_attn_tc.cuh"
 
 namespace sdva {
 namespace {
@@ -455,7 +456,8 @@ extern "C" size_t verify_attn_workspace_size(int num_lanes, int window, int num_
   if (num_sms == 0) num_sms = device_sm_count();
   VerifyPlan plan;
   if (!make_plan(num_lanes, window, num_q_heads, num_kv_heads, max_context, num_sms, &plan)) return 0;
-  return plan.bytes;
+  // enough for either kernel family (the cache dtype is not an argument here)
+  return max(plan.bytes, tc::tc_workspace_bytes(num_lanes, window, num_q_heads, num_kv_heads, num_sms));
 }
 
 extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
@@ -479,8 +481,38 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   if (!make_plan(num_lanes, window, num_q_heads, cache->num_kv_heads, max_context, num_sms, &plan))
     return SDVA_ERR_INVALID;
   if (plan.units > 65535 || plan.row_blocks > 65535) return SDVA_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < plan.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return SDVA_ERR_WORKSPACE;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SDVA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (tc::tc_supported(cache, num_lanes, window, num_q_heads, num_sms)) {
+    // FP8 cache, <= 128 rows per kv head: tcgen05 kernels
+    if (workspace_bytes < tc::tc_workspace_bytes(num_lanes, window, num_q_heads, cache->num_kv_heads, num_sms))
+      return SDVA_ERR_WORKSPACE;
+    const size_t slots = (size_t)num_lanes * cache->num_kv_heads + num_sms;
+    tc::TcArgs t;
+    t.q = static_cast<const uint16_t*>(q);
+    t.page_table = page_table;
+    t.seq_lens = seq_lens;
+    t.k_scales = static_cast<const float*>(cache->k_scales);
+    t.v_scales = static_cast<const float*>(cache->v_scales);
+    t.ws_ml = reinterpret_cast<float2*>(workspace);
+    t.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                      (slots * plan.R * sizeof(float2) + 255) / 256 * 256);
+    t.out = static_cast<uint16_t*>(out);
+    t.status = status;
+    t.num_pages = cache->num_pages;
+    t.B = num_lanes;
+    t.Hkv = cache->num_kv_heads;
+    t.Hq = num_q_heads;
+    t.G = num_q_heads / cache->num_kv_heads;
+    t.W = window;
+    t.R = plan.R;
+    t.max_pages = max_pages_per_lane;
+    t.max_context = max_context;
+    t.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    return tc::launch_verify_tc(cache, t, num_sms, s);
+  }
+  if (workspace_bytes < plan.bytes) return SDVA_ERR_WORKSPACE;
 
   VerifyArgs a;
   a.k_codes = static_cast<const uint8_t*>(cache->k_codes);
@@ -506,7 +538,6 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   a.max_splits = plan.max_splits;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid(plan.max_splits, plan.units, plan.row_blocks);
   const int threads = plan.warps * 32;
   if (cache->dtype == SDVA_KV_FP8_E4M3) {

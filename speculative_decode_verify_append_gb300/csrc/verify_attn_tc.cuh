@@ -1,0 +1,38 @@
+// verify_attn_tc.cuh -- internal interface between the verify_attn entry
+// point and the tcgen05 (FP8) kernels of verify_attn_tc.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sdva.h"
+
+namespace sdva {
+namespace tc {
+
+constexpr int kMaxLanesTc = 1024;  // lanes per call handled by the tcgen05 path
+
+struct TcArgs {
+  const uint16_t* q;  // bf16 [B][W][Hq][128]
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const float* k_scales;  // [pages][Hkv]
+  const float* v_scales;
+  float2* ws_ml;  // [lanes * Hkv + ctas][R]
+  float* ws_o;    // [lanes * Hkv + ctas][R][128]
+  uint16_t* out;  // bf16 [B][W][Hq][128]
+  int32_t* status;
+  int num_pages, B, Hkv, Hq, G, W, R, max_pages, max_context;
+  float sm_scale_log2;
+};
+
+// Scratch bytes of the tcgen05 path (split-K partials, one slot per unit and per CTA).
+size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms);
+// Whether the tcgen05 path handles this call (FP8 cache, <= 128 rows per kv head, ...).
+bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms);
+// Enqueue the split and merge kernels on `stream`.
+int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream);
+
+}  // namespace tc
+}  // namespace sdva
