@@ -200,6 +200,7 @@ int verify_attn_noalloc(const sdva_kv_cache* cache, const void* q, int num_q_hea
  *               out_tokens[b][a].
  *   seq_lens_inout: nullable int32 [num_lanes] (in/out): when given, the
  *               commit adds 1 + a to each lane's length.
+ * window: 1 .. 16 (SDVA_ERR_UNSUPPORTED above), num_lanes <= 65535.
  * An out-of-vocabulary draft id never matches and sets SDVA_STATUS_BAD_DRAFT.
  * Returns SDVA_OK or a negative SDVA_ERR_*.
  */

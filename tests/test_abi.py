@@ -114,3 +114,4 @@ def test_argument_validation_returns_before_cuda(lib):
     sa.restype = ctypes.c_int
     assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
     assert sa(fake, 0, 4, 100, fake, fake, fake, None, None, None) == -1
+    assert sa(fake, 1, 17, 100, fake, fake, fake, None, None, None) == -2

@@ -1,0 +1,65 @@
+"""The benchmark's multi-process path on CPU (gloo, world size 2): every rank
+runs an independent replica, the timed region is bracketed by barriers, and
+the job time is the maximum over ranks -- the same helpers bench.py uses
+under torchrun with NCCL on GPUs."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    import bench
+    w, r, lr = bench.dist_env()
+    dist = bench.init_dist(w, "gloo")
+    bench.barrier(dist)
+    got = bench.max_over_ranks(dist, 10.0 * (rank + 1))
+    bench.barrier(dist)
+    q.put((rank, w, r, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [x[0] for x in res] == [0, 1]
+    assert all(x[1] == 2 for x in res)
+    assert all(x[3] == 20.0 for x in res)  # every rank sees the slowest rank's time
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.init_dist(1, "gloo") is None
+    assert bench.max_over_ranks(None, 3.5) == 3.5
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    args = bench.argparse.Namespace(workload="tiny", steps=1, warmup=3, gpus=2)
+    assert bench.run_reference(args) == 0
+    assert capsys.readouterr().out == ""
