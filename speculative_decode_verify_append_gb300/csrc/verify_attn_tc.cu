@@ -4,37 +4,43 @@
 // Computes the same thing as the mma.sync path in verify_attn.cu (see there
 // and sdva.h): every window row attends over keys 0 .. L_b + i of its kv head.
 //
-// Design (one persistent CTA of 6 warps per SM):
+// Design (one persistent CTA of 16 warps per SM):
 //   * Work = the flattened list of (lane, kv head, page) triples, cut into
 //     one equal contiguous range per CTA (computed on the device from
 //     seq_lens, so the launch shape depends only on host arguments).  A
 //     maximal run of one (lane, kv head) inside a range is a "segment"; a
 //     segment that is a whole unit writes the final bf16 rows, otherwise it
-//     writes (m, l, O) partials that verify_merge_tc_kernel combines.  A
-//     segment is processed in blocks of up to 4 pages (256 keys).
-//   * Warp 4 (producer): TMA-loads each page's K tile into a ring of 4-page
-//     blocks (so a block is one contiguous 256-row operand) and its V tile
-//     into a ring of page slots (128-byte swizzle), and stages the page's
-//     scale terms.
-//   * Warp 5 (MMA): one thread issues tcgen05.mma kind::f8f6f4:
-//       S[256 keys] = Q_hi K^T + Q_lo K^T   (A = Q from shared memory,
-//                                            B = the block's K tiles, N = 256)
-//       O += P_hi V + P_lo V                (A = P from tensor memory,
-//                                            B = the page's V tile, MN-major)
-//     The tensor core streams the 128 rows of A once per instruction, so
-//     S is computed 4 pages per instruction; the K/V codes feed it as they
-//     are stored, and Q and P are each carried as the sum of two E4M3 terms
-//     (hi + lo, 8 significant bits, like bf16).
-//   * Warps 0-3 (softmax): thread t owns query row t (TMEM lane t).  Per page
-//     it reads its 64 scores, applies the page's K scale and the row's Q
-//     scale, masks the window's future keys, runs the online softmax in the
-//     log2 domain (the page's V scale folded into the shift), rescales O in
-//     tensor memory only when the running max outgrows a lag of kTau, and
-//     writes P (hi, lo) to the page's tensor-memory slot.  It releases S as
-//     soon as the block's last scores are in registers, so the next block's
-//     QK overlaps the rest of the softmax and the PVs.
+//     writes (m, l, O) partials that verify_merge_tc_kernel combines.
+//   * Pages alternate between two softmax warpgroups by the parity of their
+//     position in the CTA's range.  Each warpgroup has its own S, P and O in
+//     tensor memory and its own running (m, l); at the end of a segment
+//     warpgroup 0 combines both halves.
+//   * Warp 8 (producer): TMA-loads each page's K and V tiles (8 KB each,
+//     128-byte swizzle) into a ring of shared-memory stages, and stages the
+//     page's scale terms.
+//   * Warps 12-15 (converters): widen each page's V codes to fp16 (exact)
+//     into a second ring, laid out as the MN-major operand of the PV MMA.
+//   * Warps 9-11 issue tcgen05.mma, one thread each:
+//       warp 9 + j: S_j  = Q_hi K^T + Q_lo K^T  (kind::f8f6f4; A = Q from tensor
+//                                                memory, B = the page's K tile)
+//       warp 11:    O_j += P_j V                (kind::f16; A = P_j from tensor
+//                                                memory, B = the fp16 V tile)
+//     A thread waits on the order of a hundred cycles per tcgen05.mma it
+//     issues, whatever the tile's N, so a page's twelve instructions are
+//     spread over three issuing warps; the tensor core interleaves their
+//     streams.  Q is carried as the sum of two E4M3 terms (hi + lo, 8
+//     significant bits, like bf16); the K codes feed the tensor core as they
+//     are stored.
+//   * Warps 0-3 / 4-7 (softmax warpgroup 0 / 1): thread t owns TMEM lane t =
+//     query row t.  Per page it reads its 64 scores, applies the page's K
+//     scale and the row's Q scale, masks the window's future keys, runs the
+//     online softmax in the log2 domain (the page's V scale folded into the
+//     shift), rescales its O in tensor memory only when the running max
+//     outgrows a lag of kTau, and writes P as fp16 back to tensor memory.
+//     It releases S as soon as the scores are in registers, so the QK of its
+//     next page overlaps the rest of the softmax.
 //   * Every wait is bounded; on timeout the CTA raises SDVA_STATUS_TIMEOUT,
-//     drains its own copies, frees tensor memory and returns.
+//     drains its own copies and MMAs, frees tensor memory and returns.
 #include "tc_primitives.cuh"
 #include "verify_attn_tc.cuh"
 
@@ -42,44 +48,57 @@ namespace sdva {
 namespace tc {
 namespace {
 
-constexpr int kPagesPerBlock = 4;
-constexpr int kKBlocks = 3;    // K ring: blocks of 4 page tiles
-constexpr int kVStages = 10;   // V ring: page tiles
-constexpr int kTileBytes = 8192;  // one (page, kv head) of FP8 codes: 64 rows x 128 B
-constexpr int kKBlockBytes = kPagesPerBlock * kTileBytes;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
-// shared memory (offsets from the 1024-byte aligned base)
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kKBlocks * kKBlockBytes;
-constexpr uint32_t kOffQ = kOffV + kVStages * kTileBytes;
-constexpr uint32_t kQTermBytes = 128 * 128;  // 128 rows x 128 E4M3 codes, 128-byte swizzle
-constexpr uint32_t kOffCtl = kOffQ + 2 * kQTermBytes;
+constexpr int kStages = 8;
+constexpr int kStageBytes = 16384;   // K tile + V tile of one (page, kv head)
+constexpr int kTileBytes = 8192;     // 64 rows x 128 E4M3 codes
+constexpr int kV16Stages = 4;
+constexpr int kV16Bytes = 16384;     // fp16 V of one page: dims 0-63 | dims 64-127, 64 rows x 128 B each
+constexpr int kProducerWarp = 8;
+constexpr int kQkWarp = 9;           // + warpgroup index
+constexpr int kPvWarp = 11;
+constexpr int kConvWarp = 12;        // converters: warps 12-15
+constexpr int kThreads = 16 * 32;
+// shared memory: the fp16 V ring first, then the K/V stages, then Ctl
+constexpr uint32_t kOffV16 = 0;
+constexpr uint32_t kOffStages = kOffV16 + kV16Stages * kV16Bytes;
+constexpr uint32_t kOffCtl = kOffStages + kStages * kStageBytes;
+// Register split: launched at 128 per thread (65536 for the block); the two
+// softmax warpgroups grow to kRegsSoftmax, the other two shrink to kRegsOther.
+constexpr int kRegsSoftmax = 176;
+constexpr int kRegsOther = 80;
+static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther <= kThreads * 128, "register split");
 // tensor memory columns
-constexpr uint32_t kColS = 0;  // S: 256 fp32 columns (4 pages x 64 keys)
-__host__ __device__ constexpr uint32_t col_p(int k) { return 256u + 32u * k; }  // P slot k: hi 16 + lo 16 cols
-constexpr uint32_t kColO = 384;  // O: 128 fp32 columns
+constexpr uint32_t kColQ = 0;  // Q hi: 32 cols, Q lo: 32 cols
+__host__ __device__ constexpr uint32_t col_s(int j) { return 64u + 64u * j; }    // 64 fp32 cols
+__host__ __device__ constexpr uint32_t col_p(int j) { return 192u + 32u * j; }   // hi 16 + lo 16 cols
+__host__ __device__ constexpr uint32_t col_o(int j) { return 256u + 128u * j; }  // 128 fp32 cols
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescPV = idesc_e4m3(128, 128, 1);
-constexpr float kTau = 2.0f;      // allowed lag of the running max (log2 units)
-constexpr float kPScale = 64.0f;  // P' = softmax weight * 2^(8 - kTau) <= 256
+constexpr uint32_t kIdescQK = idesc_e4m3(128, 64, 0);
+constexpr uint32_t kIdescPV = idesc_f16(128, 128, 1);
+constexpr float kTau = 8.0f;       // allowed lag of the running max (log2 units)
+constexpr float kPScale = 128.0f;  // P' = softmax weight * 2^(15 - kTau) <= 2^15 (fp16)
+constexpr int kBarWg1Done = 1;    // named barriers between the two softmax warpgroups
+constexpr int kBarWg0Done = 2;
 
 struct Ctl {
-  uint64_t kfull[kKBlocks];
-  uint64_t kempty[kKBlocks];
-  uint64_t vfull[kVStages];
-  uint64_t vempty[kVStages];
-  uint64_t s_full;  // QK of the current block is in S
-  uint64_t s_free;  // the softmax has copied the block's S to registers
-  uint64_t p_full[kPagesPerBlock];   // P slot k written
-  uint64_t pv_done[kPagesPerBlock];  // PV that read P slot k has completed
-  uint64_t q_full;
-  float sk[kVStages];     // K scale of the page in V slot s
-  float shift[kVStages];  // log2 of its V scale (0 when the scale is 0)
-  float inv_v[kVStages];  // 1 / V scale (1 when the scale is 0)
+  uint64_t full[kStages];   // TMA bytes of the stage landed
+  uint64_t empty[kStages];  // the stage's K was used by QK, its V converted, its scales read
+  uint64_t v16_full[kV16Stages];   // fp16 V written (one arrival per converter warp)
+  uint64_t v16_empty[kV16Stages];  // the PV that read it completed
+  uint64_t s_full[2];       // QK of warpgroup j's current page is in S_j
+  uint64_t s_free[2];       // warpgroup j has copied S_j to registers
+  uint64_t p_full[2];       // warpgroup j wrote P_j
+  uint64_t pv_done[2];      // the PV that read P_j has completed
+  uint64_t q_full;          // warpgroup 0 wrote the segment's Q
+  uint64_t q_free;          // both QK issuers are done with the segment (2 arrivals)
+  float sk[kStages];        // K scale of the page in stage s
+  float shift[kStages];     // log2 of its V scale (0 when the scale is 0)
+  float inv_v[kStages];     // 1 / V scale (1 when the scale is 0)
+  float m1[128];            // warpgroup 1's running max / sum at the end of a segment
+  float l1[128];
   uint32_t tmem_base;
   int abort;
+  int stop;                   // set by warpgroup 0 at a segment end when the CTA gives up
   int pref[kMaxLanesTc + 1];  // pages per kv head of lanes < b (prefix)
   int lens[kMaxLanesTc];      // L_b
 };
@@ -117,7 +136,7 @@ struct PageIter {
     } while (b < B && pref[b + 1] == pref[b]);
     if (b < B) nb = pref[b + 1] - pref[b];
   }
-  // from the first page of a segment to the first page of the next unit
+  // from any page of a segment to the first page of the next unit
   __device__ void next_unit(const int* pref, int B, int Hkv) {
     p = nb - 1;
     next(pref, B, Hkv);
@@ -128,16 +147,13 @@ __device__ __forceinline__ void fail(Ctl* ctl, int32_t* status) {
   if (atomicExch(&ctl->abort, 1) == 0) raise_status(status, SDVA_STATUS_TIMEOUT);
 }
 
-__device__ __forceinline__ int block_pages(long long seg_len, int t) {
-  return (int)min((long long)kPagesPerBlock, seg_len - (long long)kPagesPerBlock * t);
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Two weights -> the hi and lo E4M3 bytes of each (P' = hi + lo to ~8 bits).
-__device__ __forceinline__ void split_pair(float w0, float w1, uint32_t& hi2, uint32_t& lo2) {
-  const uint32_t h = pack_f16x2(w0, w1);
-  hi2 = e4m3x2_from_f16x2(h);
-  lo2 = e4m3x2_from_f16x2(hsub2_u32(h, f16x2_from_e4m3x2(hi2)));
-}
+// first position >= g of warpgroup j's pages (positions of parity j)
+__device__ __forceinline__ long long first_own(long long g, int j) { return g + ((g ^ (long long)j) & 1); }
 
 // Row exponent e of a Q row: 2^e * max|q| lies in [128, 256).
 __device__ __forceinline__ int q_row_exponent(const uint16_t* qrow) {
@@ -156,33 +172,27 @@ __device__ __forceinline__ int q_row_exponent(const uint16_t* qrow) {
   return max(-100, min(100, 8 - k2));
 }
 
-// The Q row scaled by 2^e, split into hi + lo E4M3 codes and stored to row
-// `row` of the two shared-memory operand tiles (128-byte swizzle: 16-byte
-// chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row stores zeros.
-__device__ __forceinline__ void store_q_row_smem(const uint16_t* qrow, int e, uint8_t* qhi, uint8_t* qlo, int row) {
+// Half `half` (dims 64 * half .. + 63) of the Q row scaled by 2^e, split into
+// hi + lo E4M3 codes, packed 4 per word (word w = dims 64 * half + 4w .. + 3,
+// lowest byte first).  A null row gives zeros.
+__device__ __forceinline__ void split_q_half(const uint16_t* qrow, int e, int half, uint32_t (&hi)[16],
+                                             uint32_t (&lo)[16]) {
   const float up = ldexpf(1.0f, e);
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
-    uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qrow) v = reinterpret_cast<const uint4*>(qrow)[c * 2 + k];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int k = 0; k < 8; ++k) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (qrow) v = reinterpret_cast<const uint4*>(qrow)[8 * half + k];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int t = 0; t < 4; t += 2) {
-        const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
-        const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
-        const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
-        const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
-        const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y), l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
-        hw[2 * k + (t >> 1)] = h01 | (h23 << 16);
-        lw[2 * k + (t >> 1)] = l01 | (l23 << 16);
-      }
+    for (int t = 0; t < 4; t += 2) {
+      const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
+      const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
+      const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+      const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
+      const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y), l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
+      hi[2 * k + (t >> 1)] = h01 | (h23 << 16);
+      lo[2 * k + (t >> 1)] = l01 | (l23 << 16);
     }
-    const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
-    *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }
 
@@ -221,38 +231,48 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     }
     if (lane == 0) ctl->pref[a.B] = carry;
   }
-  const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);  // softmax threads that own rows
+  // only the softmax warps that own query rows take part in the page protocol
+  const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kKBlocks; ++s) {
-      mbar_init(smem_u32(&ctl->kfull[s]), 1);
-      mbar_init(smem_u32(&ctl->kempty[s]), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1 + 4 + row_threads / 32);  // QK commit, converters, softmax warps
     }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(smem_u32(&ctl->vfull[s]), 1);
-      mbar_init(smem_u32(&ctl->vempty[s]), 1);
+    for (int t = 0; t < kV16Stages; ++t) {
+      mbar_init(smem_u32(&ctl->v16_full[t]), 4);
+      mbar_init(smem_u32(&ctl->v16_empty[t]), 1);
     }
-    mbar_init(smem_u32(&ctl->s_full), 1);
-    mbar_init(smem_u32(&ctl->s_free), row_threads);
-    for (int k = 0; k < kPagesPerBlock; ++k) {
-      mbar_init(smem_u32(&ctl->p_full[k]), row_threads);
-      mbar_init(smem_u32(&ctl->pv_done[k]), 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_u32(&ctl->s_full[j]), 1);
+      mbar_init(smem_u32(&ctl->s_free[j]), row_threads);
+      mbar_init(smem_u32(&ctl->p_full[j]), row_threads);
+      mbar_init(smem_u32(&ctl->pv_done[j]), 1);
     }
     mbar_init(smem_u32(&ctl->q_full), row_threads);
+    mbar_init(smem_u32(&ctl->q_free), 2);
     ctl->abort = 0;
+    ctl->stop = 0;
     mbar_fence_init();
   }
   __syncthreads();
   const long long total = (long long)a.Hkv * ctl->pref[a.B];
-  const long long start = cta_start(c, C, total), end = cta_start(c + 1, C, total);
+  // pages are spread over min(C, total) CTAs, so every CTA of that set owns at least one
+  const long long Ce = min((long long)C, total);
+  const long long start = c < Ce ? cta_start(c, Ce, total) : 0, end = c < Ce ? cta_start(c + 1, Ce, total) : 0;
   const long long n_local = end - start;
   if (n_local <= 0) return;  // uniform for the whole CTA
 
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+  if (warp == kProducerWarp) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
-
+  const uint32_t stages = base + kOffStages;
+  const uint32_t v16 = base + kOffV16;
+  // Each warpgroup changes its register budget as a whole, before its warps
+  // take their roles.
+  if (warp >= 8) {
+  regs_decrease<kRegsOther>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------
     // producer: page ids and scales prefetched 32 pages at a time, two
@@ -277,10 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     locate(32 + lane, rc_b, ph_b);
     float sk_a = ph_a >= 0 ? a.k_scales[ph_a] : 0.0f;
     float sv_a = ph_a >= 0 ? a.v_scales[ph_a] : 0.0f;
-    PageIter it;
-    it.seek(start, ctl->pref, a.B, a.Hkv);
-    long long seg_left = 0, bi = 0;
-    int blk_left = 0, kk = 0;
     long long issued = 0;
     bool ok = true;
     for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
@@ -296,37 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const float sk = __shfl_sync(0xffffffffu, sk_a, i);
         const float sh = __shfl_sync(0xffffffffu, shift_a, i);
         const float iv = __shfl_sync(0xffffffffu, inv_a, i);
-        if (seg_left == 0) seg_left = min((long long)(it.nb - it.p), n_local - g);
-        const int bs = (int)(bi % kKBlocks);
-        if (blk_left == 0) {
-          // a new block of up to 4 pages of this segment
-          blk_left = (int)min((long long)kPagesPerBlock, seg_left);
-          kk = 0;
-          if (bi >= kKBlocks &&
-              !(ok = mbar_wait(smem_u32(&ctl->kempty[bs]), (uint32_t)((bi / kKBlocks - 1) & 1), abort_flag)))
-            break;
-          if (lane == 0) mbar_arrive_expect_tx(smem_u32(&ctl->kfull[bs]), (uint32_t)blk_left * kTileBytes);
-        }
-        const int vs = (int)(g % kVStages);
-        if (g >= kVStages &&
-            !(ok = mbar_wait(smem_u32(&ctl->vempty[vs]), (uint32_t)((g / kVStages - 1) & 1), abort_flag)))
+        const int s = (int)(g % kStages);
+        if (g >= kStages && !(ok = mbar_wait(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
           break;
         if (lane == 0) {
-          ctl->sk[vs] = sk;
-          ctl->shift[vs] = sh;
-          ctl->inv_v[vs] = iv;
-          const uint32_t vbar = smem_u32(&ctl->vfull[vs]);
-          mbar_arrive_expect_tx(vbar, kTileBytes);
-          tma_load_2d(base + kOffV + vs * kTileBytes, &map_v, 0, rc, vbar);
-          tma_load_2d(base + kOffK + bs * kKBlockBytes + kk * kTileBytes, &map_k, 0, rc,
-                      smem_u32(&ctl->kfull[bs]));
+          ctl->sk[s] = sk;
+          ctl->shift[s] = sh;
+          ctl->inv_v[s] = iv;
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(bar, kStageBytes);
+          tma_load_2d(stages + s * kStageBytes, &map_k, 0, rc, bar);
+          tma_load_2d(stages + s * kStageBytes + kTileBytes, &map_v, 0, rc, bar);
         }
         __syncwarp();
         issued = g + 1;
-        ++kk;
-        --seg_left;
-        if (--blk_left == 0) ++bi;
-        it.next(ctl->pref, a.B, a.Hkv);
       }
       rc_a = rc_b;
       sk_a = sk_b;
@@ -337,301 +336,402 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     if (!ok) {
       fail(ctl, a.status);
       // drain this CTA's own copies still in flight (bounded)
-      for (long long g = max(0LL, issued - kVStages); g < issued; ++g) {
+      for (long long g = max(0LL, issued - kStages); g < issued; ++g) {
         int dummy = 0;
-        mbar_wait(smem_u32(&ctl->vfull[g % kVStages]), (uint32_t)((g / kVStages) & 1), &dummy, 400000000LL);
+        mbar_wait(smem_u32(&ctl->full[g % kStages]), (uint32_t)((g / kStages) & 1), &dummy, 400000000LL);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kQkWarp || warp == kQkWarp + 1) {
     // ------------------------------------------------------------------
-    // MMA issuer.  Per block: the PVs of the pages before its last pair,
-    // then (within a segment) the next block's QK as soon as S is free, then
-    // the PVs of the last pair.  All PVs of a segment are issued before the
-    // next segment's Q is awaited.
+    // QK issuer of warpgroup j: S_j = Q K^T for the warpgroup's pages, each
+    // as soon as its K tile has landed and the warpgroup has copied out the
+    // scores of its previous page.
     // ------------------------------------------------------------------
+    const int j = warp - kQkWarp;
     PageIter it;
     it.seek(start, ctl->pref, a.B, a.Hkv);
     uint32_t q_phase = 0;
-    uint32_t slot_use[kPagesPerBlock] = {0u, 0u, 0u, 0u};
     bool ok = true;
-    long long last_pv = -1;
-    const uint32_t qhi = base + kOffQ, qlo = base + kOffQ + kQTermBytes;
-    auto issue_qk = [&](long long b, int npg) -> bool {
-      const int bs = (int)(b % kKBlocks);
-      if (!mbar_wait(smem_u32(&ctl->kfull[bs]), (uint32_t)((b / kKBlocks) & 1), abort_flag)) return false;
-      if (b > 0 && !mbar_wait(smem_u32(&ctl->s_free), (uint32_t)((b - 1) & 1), abort_flag)) return false;
-      fence_after_sync();
-      if (lane == 0) {
-        const uint32_t kblk = base + kOffK + bs * kKBlockBytes;
-        const uint32_t idesc = idesc_e4m3(128, 64 * npg, 0);
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_e4m3_ss(tmem + kColS, sdesc_sw128((half ? qlo : qhi) + 32 * k, 1024, 1024),
-                        sdesc_sw128(kblk + 32 * k, 1024, 1024), idesc, (half == 0 && k == 0) ? 0u : 1u);
-        mma_commit(smem_u32(&ctl->s_full));
-        mma_commit(smem_u32(&ctl->kempty[bs]));
-      }
-      __syncwarp();
-      return true;
-    };
-    auto issue_pv = [&](long long gp, int k, bool first_of_seg) -> bool {
-      const int vs = (int)(gp % kVStages);
-      if (!mbar_wait(smem_u32(&ctl->vfull[vs]), (uint32_t)((gp / kVStages) & 1), abort_flag)) return false;
-      if (!mbar_wait(smem_u32(&ctl->p_full[k]), slot_use[k] & 1u, abort_flag)) return false;
-      fence_after_sync();
-      if (lane == 0) {
-        const uint32_t vtile = base + kOffV + vs * kTileBytes;
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_e4m3_ts(tmem + kColO, tmem + col_p(k) + 16 * half + 8 * kk,
-                        sdesc_sw128(vtile + 4096 * kk, 1024, 1024), kIdescPV,
-                        (first_of_seg && half == 0 && kk == 0) ? 0u : 1u);
-        mma_commit(smem_u32(&ctl->pv_done[k]));
-        mma_commit(smem_u32(&ctl->vempty[vs]));
-      }
-      __syncwarp();
-      ++slot_use[k];
-      last_pv = gp;
-      return true;
-    };
-    long long g = 0, bi = 0;
+    long long last = -1;
+    long long g = 0;
     while (g < n_local && ok) {
-      const long long s0 = g, seg_len = min((long long)(it.nb - it.p), n_local - g);
-      const int nblk = (int)((seg_len + kPagesPerBlock - 1) / kPagesPerBlock);
+      const long long seg_len = min((long long)(it.nb - it.p), n_local - g);
       if (!(ok = mbar_wait(smem_u32(&ctl->q_full), q_phase, abort_flag))) break;
       q_phase ^= 1u;
-      if (!(ok = issue_qk(bi, block_pages(seg_len, 0)))) break;
-      for (int t = 0; t < nblk && ok; ++t, ++bi) {
-        const int npg = block_pages(seg_len, t);
-        const long long g0 = s0 + (long long)kPagesPerBlock * t;
-        const int last_pair = npg > 2 ? 2 : 0;
-        for (int k = 0; k < last_pair && ok; ++k) ok = issue_pv(g0 + k, k, g0 + k == s0);
-        if (ok && t + 1 < nblk) ok = issue_qk(bi + 1, block_pages(seg_len, t + 1));
-        for (int k = last_pair; k < npg && ok; ++k) ok = issue_pv(g0 + k, k, g0 + k == s0);
+      for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
+        const int s = (int)(h % kStages);
+        if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
+        if (h >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[j]), (uint32_t)(((h - 2) >> 1) & 1), abort_flag)))
+          break;
+        fence_after_sync();
+        if (lane == 0) {
+          const uint32_t ktile = stages + s * kStageBytes;
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3_ts(tmem + col_s(j), tmem + kColQ + 32 * half + 8 * k, sdesc_sw128(ktile + 32 * k, 1024, 1024),
+                          kIdescQK, (half == 0 && k == 0) ? 0u : 1u);
+          mma_commit(smem_u32(&ctl->s_full[j]));
+          mma_commit(smem_u32(&ctl->empty[s]));
+        }
+        __syncwarp();
+        last = h;
       }
+      if (!ok) break;
+      // every QK of this segment is issued: warpgroup 0 may load the next Q
+      // once the other issuer is done too (and the softmax has consumed S)
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->q_free));
+      __syncwarp();
+      g += seg_len;
       it.next_unit(ctl->pref, a.B, a.Hkv);
-      g = s0 + seg_len;
     }
     if (!ok) {
       fail(ctl, a.status);
       // let the tensor core finish what this thread issued before tensor memory is freed
-      if (last_pv >= 0) {
+      if (last >= 0) {
         int dummy = 0;
-        mbar_wait(smem_u32(&ctl->vempty[last_pv % kVStages]), (uint32_t)((last_pv / kVStages) & 1), &dummy,
+        mbar_wait(smem_u32(&ctl->s_full[j]), (uint32_t)((last >> 1) & 1), &dummy, 400000000LL);
+      }
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------------
+    // PV issuer: O_j += P_j V for every page in order (j = its warpgroup);
+    // a warpgroup's first page of a segment starts its O_j afresh.
+    // ------------------------------------------------------------------
+    PageIter it;
+    it.seek(start, ctl->pref, a.B, a.Hkv);
+    bool ok = true;
+    long long last = -1;
+    long long g = 0;
+    while (g < n_local && ok) {
+      const long long seg_len = min((long long)(it.nb - it.p), n_local - g);
+      bool fresh0 = true, fresh1 = true;
+      for (long long h = g; h < g + seg_len; ++h) {
+        const int j = (int)(h & 1), t = (int)(h % kV16Stages);
+        const bool fresh = j ? fresh1 : fresh0;
+        if (!(ok = mbar_wait(smem_u32(&ctl->p_full[j]), (uint32_t)((h >> 1) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag))) break;
+        fence_after_sync();
+        if (lane == 0) {
+          const uint32_t vt = v16 + t * kV16Bytes;
+          // B: 16 keys per instruction (2048 bytes of both dim halves), the
+          // two 64-dim halves 8192 bytes apart (leading byte offset), 8-key
+          // groups 1024 bytes apart (stride byte offset)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16_ts(tmem + col_o(j), tmem + col_p(j) + 8 * k, sdesc_sw128(vt + 2048 * k, 8192, 1024), kIdescPV,
+                       (fresh && k == 0) ? 0u : 1u);
+          mma_commit(smem_u32(&ctl->pv_done[j]));
+          mma_commit(smem_u32(&ctl->v16_empty[t]));
+        }
+        __syncwarp();
+        (j ? fresh1 : fresh0) = false;
+        last = h;
+      }
+      g += seg_len;
+      it.next_unit(ctl->pref, a.B, a.Hkv);
+    }
+    if (!ok) {
+      fail(ctl, a.status);
+      if (last >= 0) {
+        int dummy = 0;
+        mbar_wait(smem_u32(&ctl->v16_empty[last % kV16Stages]), (uint32_t)((last / kV16Stages) & 1), &dummy,
                   400000000LL);
       }
     }
-  } else if (warp < 4 && warp * 32 < a.R) {
+  } else if (warp >= kConvWarp) {
     // ------------------------------------------------------------------
-    // softmax: thread = query row = TMEM lane (warps without rows idle)
+    // converters: page g's V codes (TMA tile, 128-byte swizzle, row = key)
+    // -> fp16 in V16 slot g % kV16Stages: dims 0-63 and 64-127 as two
+    // 64-row x 128-byte regions, each with the 128-byte swizzle (16-byte
+    // chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  E4M3 -> fp16 is
+    // exact.  Thread u handles the 16-byte source chunks u, u + 128, ...
     // ------------------------------------------------------------------
-    const int row = threadIdx.x;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int u = threadIdx.x - kConvWarp * 32;
+    bool ok = true;
+    for (long long h = 0; h < n_local && ok; ++h) {
+      const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
+      if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
+      if (h >= kV16Stages &&
+          !(ok = mbar_wait(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+        break;
+      const uint8_t* src = base_ptr + kOffStages + s * kStageBytes + kTileBytes;
+      uint8_t* dst = base_ptr + kOffV16 + t * kV16Bytes;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int item = u + 128 * q;
+        const int r = item >> 3, c = item & 7;  // key row, 16-dim chunk
+        const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+        const uint32_t b[4] = {w.x, w.y, w.z, w.w};
+        uint32_t h16[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          h16[2 * k] = f16x2_from_e4m3x2(b[k] & 0xFFFFu);
+          h16[2 * k + 1] = f16x2_from_e4m3x2(b[k] >> 16);
+        }
+        // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
+        uint8_t* reg = dst + (c >> 2) * 8192 + r * 128;
+        const int c0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(reg + (((c0) ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+        *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+      }
+      // generic-proxy writes -> visible to the tensor core
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->v16_full[t]));
+        mbar_arrive(smem_u32(&ctl->empty[s]));
+      }
+    }
+    if (!ok) fail(ctl, a.status);
+  }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------------------
+    // softmax warpgroups: wg 0 = warps 0-3 (even positions), wg 1 = warps
+    // 4-7 (odd positions); thread = query row = TMEM lane
+    // ------------------------------------------------------------------
+    const int wg = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const bool warp_active = (warp & 3) * 32 < a.R;
     const bool row_valid = row < a.R;
     const int i_row = row_valid ? row / a.G : a.W - 1;
-    uint8_t* qhi = base_ptr + kOffQ;
-    uint8_t* qlo = base_ptr + kOffQ + kQTermBytes;
     PageIter it;
     it.seek(start, ctl->pref, a.B, a.Hkv);
-    uint32_t slot_use[kPagesPerBlock] = {0u, 0u, 0u, 0u};
-    long long g = 0, bi = 0;
-    int last_slot = -1;
-    uint32_t last_use = 0;
+    long long g = 0;
+    uint32_t seg_count = 0;
     bool ok = true;
-    while (g < n_local && ok) {
-      // ---- segment setup: Q of this (lane, kv head) into shared memory ----
+    while (g < n_local) {
+      // ---- segment setup ----
       const int b = it.b, hk = it.hk, nb = it.nb, p0 = it.p;
       const int L = ctl->lens[b];
+      const long long g_first = g;
       const long long seg_len = min((long long)(nb - p0), n_local - g);
       const bool whole_unit = (p0 == 0) && seg_len == nb;
       const int u = b * a.Hkv + hk;
       const int h = hk * a.G + (row_valid ? row % a.G : 0);
       const uint16_t* qrow = a.q + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
       const int e = row_valid ? q_row_exponent(qrow) : 0;
-      store_q_row_smem(row_valid ? qrow : nullptr, e, qhi, qlo, row);
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&ctl->q_full));
+      if (ok && wg == 0 && warp_active) {
+        // the previous segment's QKs are all issued (and, through the
+        // segment-end handshake, complete): Q may be overwritten
+        if (seg_count > 0) ok = mbar_wait(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag);
+        if (ok) {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t hi[16], lo[16];
+            split_q_half(row_valid ? qrow : nullptr, e, half, hi, lo);
+            tmem_st16(lane_base + kColQ + 16 * half, hi);
+            tmem_st16(lane_base + kColQ + 32 + 16 * half, lo);
+            tmem_wait_st();
+          }
+          fence_before_sync();
+          mbar_arrive(smem_u32(&ctl->q_full));
+        }
+      }
+      ++seg_count;
       const float row_scale = ldexpf(a.sm_scale_log2, -e);
 
       float m = -INFINITY, l = 0.0f;
-      const int nblk = (int)((seg_len + kPagesPerBlock - 1) / kPagesPerBlock);
-      for (int t = 0; t < nblk && ok; ++t, ++bi) {
-        const int npg = block_pages(seg_len, t);
-        const long long g0 = g + (long long)kPagesPerBlock * t;
-        if (!(ok = mbar_wait(smem_u32(&ctl->s_full), (uint32_t)(bi & 1), abort_flag))) break;
+      bool had_page = false;
+      for (long long k = 0; k < seg_len && ok; ++k, ++g) {
+        if ((int)(g & 1) != wg) continue;
+        had_page = true;
+        if (!warp_active) continue;
+        const int j = wg;
+        const int p = p0 + (int)k;
+        const int s = (int)(g % kStages);
+        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[j]), (uint32_t)((g >> 1) & 1), abort_flag))) break;
+        // the producer staged the page's scale terms before completing full[s]
+        if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
         fence_after_sync();
-        for (int pair = 0; pair * 2 < npg && ok; ++pair) {
-          // the scores of up to two pages in registers
-          uint32_t xs[2][64];
-          const int k0 = 2 * pair;
-          tmem_ld32(lane_base + kColS + 64 * k0, *reinterpret_cast<uint32_t(*)[32]>(&xs[0][0]));
-          tmem_ld32(lane_base + kColS + 64 * k0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[0][32]));
-          if (k0 + 1 < npg) {
-            tmem_ld32(lane_base + kColS + 64 * (k0 + 1), *reinterpret_cast<uint32_t(*)[32]>(&xs[1][0]));
-            tmem_ld32(lane_base + kColS + 64 * (k0 + 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&xs[1][32]));
-          }
-          tmem_wait_ld();
-          if (k0 + 2 >= npg) {
-            // the block's last scores are in registers: the MMA may compute the next block's S
-            fence_before_sync();
-            mbar_arrive(smem_u32(&ctl->s_free));
-          }
-          for (int kp = 0; kp < 2 && k0 + kp < npg && ok; ++kp) {
-            const int k = k0 + kp;
-            const long long gp = g0 + k;
-            const int vs = (int)(gp % kVStages);
-            // the producer staged this page's scale terms before completing vfull
-            if (!(ok = mbar_wait(smem_u32(&ctl->vfull[vs]), (uint32_t)((gp / kVStages) & 1), abort_flag))) break;
-            const float kscale = ctl->sk[vs] * row_scale, shift = ctl->shift[vs], inv_f = ctl->inv_v[vs];
-            const uint32_t* x = xs[kp];
-            const int kbase = (p0 + kPagesPerBlock * t + k) * kPage;
-            const int lim = L + i_row;  // last visible key position of this row
-            const bool partial = kbase + kPage - 1 > lim;
-            float smax = -INFINITY;
-            if (!partial) {
-              float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-              for (int q = 0; q < 64; q += 8) {
-                m0 = fmax3(m0, __uint_as_float(x[q]), __uint_as_float(x[q + 1]));
-                m1 = fmax3(m1, __uint_as_float(x[q + 2]), __uint_as_float(x[q + 3]));
-                m2 = fmax3(m2, __uint_as_float(x[q + 4]), __uint_as_float(x[q + 5]));
-                m3 = fmax3(m3, __uint_as_float(x[q + 6]), __uint_as_float(x[q + 7]));
-              }
-              smax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-            } else {
-#pragma unroll
-              for (int q = 0; q < 64; ++q)
-                if (kbase + q <= lim) smax = fmaxf(smax, __uint_as_float(x[q]));
-            }
-            const float xmax = smax == -INFINITY ? -INFINITY : fmaf(smax, kscale, shift);
-            // The running max may lag the true one by up to kTau (log2 units):
-            // weights then reach 2^kTau and P' = w * 2^(8 - kTau) stays <= 256.
-            // O is rescaled only when some row of the warp outgrows that.
-            const bool need = m != -INFINITY && xmax > m + kTau;
-            if (__any_sync(0xffffffffu, need)) {
-              // every PV of this segment so far must be complete
-              if (!(ok = mbar_wait(smem_u32(&ctl->pv_done[last_slot]), last_use & 1u, abort_flag))) break;
-              fence_after_sync();
-              const float m_new = m == -INFINITY ? m : fmaxf(m, xmax);
-              const float alpha = (m == -INFINITY || m_new == m) ? 1.0f : fast_exp2(m - m_new);
-#pragma unroll 1
-              for (int cc = 0; cc < 4; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + kColO + 32 * cc, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-                tmem_st32(lane_base + kColO + 32 * cc, o);
-              }
-              tmem_wait_st();
-              l *= alpha;
-              m = m_new;
-            }
-            if (m == -INFINITY) m = xmax;  // first visible key of this row in the segment
-            const float bias = shift - (m == -INFINITY ? 0.0f : m) + (8.0f - kTau);
-            uint32_t phi[16], plo[16];
-            float sum;
-            if (!partial) {
-              const unsigned long long k2 = f2_pack(kscale, kscale), b2 = f2_pack(bias, bias);
-              unsigned long long acc = f2_pack(0.0f, 0.0f);
-#pragma unroll
-              for (int q = 0; q < 64; q += 4) {
-                const float2 y01 = f2_unpack(ffma2(f2_pack(__uint_as_float(x[q]), __uint_as_float(x[q + 1])), k2, b2));
-                const float2 y23 =
-                    f2_unpack(ffma2(f2_pack(__uint_as_float(x[q + 2]), __uint_as_float(x[q + 3])), k2, b2));
-                const float w0 = fast_exp2(y01.x), w1 = fast_exp2(y01.y), w2 = fast_exp2(y23.x), w3 = fast_exp2(y23.y);
-                acc = fadd2(acc, fadd2(f2_pack(w0, w1), f2_pack(w2, w3)));
-                uint32_t h01, l01, h23, l23;
-                split_pair(w0, w1, h01, l01);
-                split_pair(w2, w3, h23, l23);
-                phi[q >> 2] = __byte_perm(h01, h23, 0x5410);
-                plo[q >> 2] = __byte_perm(l01, l23, 0x5410);
-              }
-              const float2 a2 = f2_unpack(acc);
-              sum = a2.x + a2.y;
-            } else {
-              sum = 0.0f;
-#pragma unroll
-              for (int q = 0; q < 64; q += 4) {
-                float w[4];
-#pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4)
-                  w[r4] = kbase + q + r4 <= lim ? fast_exp2(fmaf(__uint_as_float(x[q + r4]), kscale, bias)) : 0.0f;
-                sum += (w[0] + w[1]) + (w[2] + w[3]);
-                uint32_t h01, l01, h23, l23;
-                split_pair(w[0], w[1], h01, l01);
-                split_pair(w[2], w[3], h23, l23);
-                phi[q >> 2] = __byte_perm(h01, h23, 0x5410);
-                plo[q >> 2] = __byte_perm(l01, l23, 0x5410);
-              }
-            }
-            l += sum * (1.0f / kPScale) * inv_f;
-            // P slot k is free once the PV of its previous use has completed
-            if (slot_use[k] > 0 &&
-                !(ok = mbar_wait(smem_u32(&ctl->pv_done[k]), (slot_use[k] - 1u) & 1u, abort_flag)))
-              break;
-            tmem_st16(lane_base + col_p(k), phi);
-            tmem_st16(lane_base + col_p(k) + 16, plo);
-            tmem_wait_st();
-            fence_before_sync();
-            mbar_arrive(smem_u32(&ctl->p_full[k]));
-            last_slot = k;
-            last_use = slot_use[k]++;
-          }
-        }
-      }
-      if (!ok) break;
-      // ---- segment epilogue: every PV of the segment must have completed ----
-      if (!(ok = mbar_wait(smem_u32(&ctl->pv_done[last_slot]), last_use & 1u, abort_flag))) break;
-      fence_after_sync();
-      const size_t slot_row = ((size_t)(u + c)) * a.R + row;
-      const float inv = (row_valid && l > 0.0f) ? 1.0f / (kPScale * l) : 0.0f;
-      uint16_t* orow = nullptr;
-      float* prow = nullptr;
-      if (row_valid) {
-        if (whole_unit)
-          orow = a.out + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
-        else {
-          prow = a.ws_o + slot_row * kHeadDim;
-          a.ws_ml[slot_row] = make_float2(m, l);
-        }
-      }
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * cc, o);
+        const float kscale = ctl->sk[s] * row_scale, shift = ctl->shift[s], inv_f = ctl->inv_v[s];
+        // the stage's scale terms are in registers: this warp's share of releasing the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
+        uint32_t x[64];
+        tmem_ld32(lane_base + col_s(j), *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(lane_base + col_s(j) + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
-        if (orow) {
+        // S_j is in registers: the issuer may compute the warpgroup's next page into it
+        fence_before_sync();
+        mbar_arrive(smem_u32(&ctl->s_free[j]));
+        const int kbase = p * kPage;
+        const int lim = L + i_row;  // last visible key position of this row
+        const bool partial = kbase + kPage - 1 > lim;
+        float smax = -INFINITY;
+        if (!partial) {
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-          for (int q = 0; q < 32; q += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[q + 4]) * inv, __uint_as_float(o[q + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[q + 6]) * inv, __uint_as_float(o[q + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * cc + q) = w;
+          for (int q = 0; q < 64; q += 8) {
+            m0 = fmax3(m0, __uint_as_float(x[q]), __uint_as_float(x[q + 1]));
+            m1 = fmax3(m1, __uint_as_float(x[q + 2]), __uint_as_float(x[q + 3]));
+            m2 = fmax3(m2, __uint_as_float(x[q + 4]), __uint_as_float(x[q + 5]));
+            m3 = fmax3(m3, __uint_as_float(x[q + 6]), __uint_as_float(x[q + 7]));
           }
-        } else if (prow) {
+          smax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        } else {
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
-            *reinterpret_cast<float4*>(prow + 32 * cc + q) =
-                make_float4(__uint_as_float(o[q]) * (1.0f / kPScale), __uint_as_float(o[q + 1]) * (1.0f / kPScale),
-                            __uint_as_float(o[q + 2]) * (1.0f / kPScale), __uint_as_float(o[q + 3]) * (1.0f / kPScale));
+          for (int q = 0; q < 64; ++q)
+            if (kbase + q <= lim) smax = fmaxf(smax, __uint_as_float(x[q]));
+        }
+        const float xmax = smax == -INFINITY ? -INFINITY : fmaf(smax, kscale, shift);
+        // P_j and O_j: the PV of the warpgroup's previous page must be done
+        if (g >= 2 && !(ok = mbar_wait(smem_u32(&ctl->pv_done[j]), (uint32_t)(((g - 2) >> 1) & 1), abort_flag)))
+          break;
+        // The running max may lag the true one by up to kTau (log2 units):
+        // weights then reach 2^kTau and P' = w * 2^(15 - kTau) stays <= 2^15,
+        // inside fp16.  O is rescaled only when some row of the warp outgrows that.
+        const bool need = m != -INFINITY && xmax > m + kTau;
+        if (__any_sync(0xffffffffu, need)) {
+          fence_after_sync();
+          const float m_new = m == -INFINITY ? m : fmaxf(m, xmax);
+          const float alpha = (m == -INFINITY || m_new == m) ? 1.0f : fast_exp2(m - m_new);
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o(j) + 32 * cc, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st32(lane_base + col_o(j) + 32 * cc, o);
+          }
+          tmem_wait_st();
+          l *= alpha;
+          m = m_new;
+        }
+        if (m == -INFINITY) m = xmax;  // first visible key of this row in the segment
+        const float bias = shift - (m == -INFINITY ? 0.0f : m) + (15.0f - kTau);
+        // P' = 2^(s * kscale + bias) as fp16; P_j column w holds keys 2w, 2w + 1
+        float sum = 0.0f;
+        const unsigned long long k2 = f2_pack(kscale, kscale), b2 = f2_pack(bias, bias);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t ph[16];
+          if (!partial) {
+            unsigned long long acc = f2_pack(0.0f, 0.0f);
+#pragma unroll
+            for (int q = 32 * hf; q < 32 * hf + 32; q += 4) {
+              const float2 y01 = f2_unpack(ffma2(f2_pack(__uint_as_float(x[q]), __uint_as_float(x[q + 1])), k2, b2));
+              const float2 y23 =
+                  f2_unpack(ffma2(f2_pack(__uint_as_float(x[q + 2]), __uint_as_float(x[q + 3])), k2, b2));
+              const float w0 = fast_exp2(y01.x), w1 = fast_exp2(y01.y), w2 = fast_exp2(y23.x), w3 = fast_exp2(y23.y);
+              acc = fadd2(acc, fadd2(f2_pack(w0, w1), f2_pack(w2, w3)));
+              ph[(q & 31) >> 1] = pack_f16x2(w0, w1);
+              ph[((q & 31) >> 1) + 1] = pack_f16x2(w2, w3);
+            }
+            const float2 a2 = f2_unpack(acc);
+            sum += a2.x + a2.y;
+          } else {
+#pragma unroll
+            for (int q = 32 * hf; q < 32 * hf + 32; q += 2) {
+              const float w0 = kbase + q <= lim ? fast_exp2(fmaf(__uint_as_float(x[q]), kscale, bias)) : 0.0f;
+              const float w1 = kbase + q + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(x[q + 1]), kscale, bias)) : 0.0f;
+              sum += w0 + w1;
+              ph[(q & 31) >> 1] = pack_f16x2(w0, w1);
+            }
+          }
+          tmem_st16(lane_base + col_p(j) + 16 * hf, ph);
+        }
+        l += sum * (1.0f / kPScale) * inv_f;
+        tmem_wait_st();
+        fence_before_sync();
+        mbar_arrive(smem_u32(&ctl->p_full[j]));
+      }
+      g = g_first + seg_len;
+      it.next_unit(ctl->pref, a.B, a.Hkv);
+      // ---- segment end: this warpgroup's last PV must have completed ----
+      if (ok && had_page && warp_active) {
+        long long g_last = g - 1;
+        if ((int)(g_last & 1) != wg) --g_last;
+        ok = mbar_wait(smem_u32(&ctl->pv_done[wg]), (uint32_t)((g_last >> 1) & 1), abort_flag);
+        fence_after_sync();
+      }
+      if (!ok) fail(ctl, a.status);
+      // Both warpgroups meet here once per segment, whatever happened, so
+      // neither waits on a named barrier the other never reaches.
+      if (wg == 1) {
+        ctl->m1[row] = (had_page && warp_active) ? m : -INFINITY;
+        ctl->l1[row] = (had_page && warp_active) ? l : 0.0f;
+        named_arrive(kBarWg1Done, 256);
+        named_sync(kBarWg0Done, 256);  // warpgroup 0 has read this warpgroup's O
+        fence_after_sync();
+        if (ctl->stop) break;
+        continue;
+      }
+      named_sync(kBarWg1Done, 256);
+      fence_after_sync();
+      const bool stop = !ok || *abort_flag;
+      const bool had0 = seg_len > 1 || (g_first & 1) == 0;  // warpgroup 0 owned a page of this segment
+      const bool had1 = seg_len > 1 || (g_first & 1) == 1;  // warpgroup 1 owned a page of this segment
+      if (warp_active && !stop) {
+        const float m0 = had0 ? m : -INFINITY, l0 = had0 ? l : 0.0f;
+        const float mm1 = ctl->m1[row], ll1 = ctl->l1[row];
+        const float M = fmaxf(m0, mm1);
+        const float a0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - M);
+        const float a1 = mm1 == -INFINITY ? 0.0f : fast_exp2(mm1 - M);
+        const float lt = a0 * l0 + a1 * ll1;
+        const size_t slot_row = ((size_t)(u + c)) * a.R + row;
+        const float inv = (row_valid && lt > 0.0f) ? 1.0f / (kPScale * lt) : 0.0f;
+        uint16_t* orow = nullptr;
+        float* prow = nullptr;
+        if (row_valid) {
+          if (whole_unit)
+            orow = a.out + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
+          else {
+            prow = a.ws_o + slot_row * kHeadDim;
+            a.ws_ml[slot_row] = make_float2(M, lt);
+          }
+        }
+        const float f0 = had0 ? a0 : 0.0f, f1 = had1 ? a1 : 0.0f;
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t o0[16], o1[16];
+          if (had0) tmem_ld16(lane_base + col_o(0) + 16 * cc, o0);
+          if (had1) tmem_ld16(lane_base + col_o(1) + 16 * cc, o1);
+          tmem_wait_ld();
+          if (!had0) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) o0[t] = 0u;
+          }
+          if (!had1) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) o1[t] = 0u;
+          }
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            o0[t] = __float_as_uint(fmaf(f0, __uint_as_float(o0[t]), f1 * __uint_as_float(o1[t])));
+          if (orow) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              pk[t] = pack_bf16x2(__uint_as_float(o0[2 * t]) * inv, __uint_as_float(o0[2 * t + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(orow + 16 * cc);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else if (prow) {
+            float4* dst = reinterpret_cast<float4*>(prow + 16 * cc);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              dst[t] = make_float4(__uint_as_float(o0[4 * t]) * (1.0f / kPScale),
+                                   __uint_as_float(o0[4 * t + 1]) * (1.0f / kPScale),
+                                   __uint_as_float(o0[4 * t + 2]) * (1.0f / kPScale),
+                                   __uint_as_float(o0[4 * t + 3]) * (1.0f / kPScale));
+          }
         }
       }
-      g += seg_len;
-      it.next_unit(ctl->pref, a.B, a.Hkv);
+      if (threadIdx.x == 0) ctl->stop = stop ? 1 : 0;
+      fence_before_sync();
+      named_arrive(kBarWg0Done, 256);
+      if (stop) break;
     }
-    if (!ok) fail(ctl, a.status);
   }
 
   fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kProducerWarp) {
     fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -645,7 +745,7 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
   const int b = u / a.Hkv, hk = u % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ int s_bad;
-  __shared__ long long s_first, s_last, s_total;
+  __shared__ long long s_first, s_last;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   const int L = a.seq_lens[b];
@@ -678,18 +778,21 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
     if (lane == 0 && len_ok) {
       const long long total = (long long)a.Hkv * all;
       const long long Pu = (long long)a.Hkv * before + (long long)hk * nb;
+      const long long Ce = min((long long)C, total);  // CTAs that own pages (each at least one)
       auto locate = [&](long long x) {
-        long long cc = x * C / total;
-        while (cc + 1 < C && cta_start(cc + 1, C, total) <= x) ++cc;
-        while (cc > 0 && cta_start(cc, C, total) > x) --cc;
+        long long cc = x * Ce / total;
+        while (cc + 1 < Ce && cta_start(cc + 1, Ce, total) <= x) ++cc;
+        while (cc > 0 && cta_start(cc, Ce, total) > x) --cc;
         return cc;
       };
       s_first = locate(Pu);
       s_last = locate(Pu + nb - 1);
-      s_total = total;
     }
   }
   __syncthreads();
+  // launched as a programmatic dependent of the split kernel: everything
+  // above overlapped its tail; its partials and rows are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bad = s_bad;
   const int r = blockIdx.y * 8 + warp;
   if (bad) {
@@ -701,23 +804,19 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
     }
     return;
   }
-  const long long c_first = s_first, c_last = s_last, total = s_total;
+  const long long c_first = s_first, c_last = s_last;
   if (c_first == c_last || r >= a.R) return;  // one segment: the split kernel wrote the rows
   const int nseg = (int)(c_last - c_first + 1);
   float M = -INFINITY;
   for (int sgi = lane; sgi < nseg; sgi += 32) {
-    const long long cc = c_first + sgi;
-    if (cta_start(cc, C, total) == cta_start(cc + 1, C, total)) continue;
-    M = fmaxf(M, a.ws_ml[(size_t)(u + cc) * a.R + r].x);
+    M = fmaxf(M, a.ws_ml[(size_t)(u + c_first + sgi) * a.R + r].x);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float den = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
   for (int sgi = 0; sgi < nseg; ++sgi) {
-    const long long cc = c_first + sgi;
-    if (cta_start(cc, C, total) == cta_start(cc + 1, C, total)) continue;
-    const size_t slot_row = (size_t)(u + cc) * a.R + r;
+    const size_t slot_row = (size_t)(u + c_first + sgi) * a.R + r;
     const float2 ml = a.ws_ml[slot_row];
     const float4 v = *reinterpret_cast<const float4*>(a.ws_o + slot_row * kHeadDim + lane * 4);
     const float w = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);
@@ -788,8 +887,17 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
   cudaFuncSetAttribute(verify_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   verify_split_tc_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(mk, mv, args);
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
-  verify_merge_tc_kernel<<<dim3(args.B * args.Hkv, (args.R + 7) / 8), 256, 0, stream>>>(args, num_sms);
-  return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(args.B * args.Hkv, (args.R + 7) / 8, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, verify_merge_tc_kernel, args, num_sms) != cudaSuccess) return SDVA_ERR_CUDA;
+  return SDVA_OK;
 }
 
 }  // namespace tc
