@@ -44,9 +44,10 @@ import synth  # noqa: E402
 SM_SCALE = np.float32(1.0 / math.sqrt(128.0))
 METRIC = "verify_attn HBM GB/s (% of GB300 peak) and verify steps/s at 8 lanes"
 DEFAULT_WORKLOAD = "multi_lane"
-# dram bytes (read + write) of one verify_attn call measured by ncu for the
-# current kernels, per workload; None until a capture of these kernels exists
-NCU_TRAFFIC_BYTES = {}
+# dram bytes (read + write) of one verify_attn call (split + merge kernels),
+# measured by ncu for the current kernels, per workload (absent: not captured
+# for this workload, reported as null).  Source: profiles/verify_split_tc_fp8_multi_lane.md
+NCU_TRAFFIC_BYTES = {"multi_lane": 305_199_000 + 652_000 + 9_187_000}
 
 
 def workload_desc(spec: synth.Spec) -> str:
