@@ -485,16 +485,18 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (tc::tc_supported(cache, num_lanes, window, num_q_heads, num_sms)) {
-    // FP8 cache, <= 128 rows per kv head: tcgen05 kernels
+    // <= 128 rows per kv head: tcgen05 kernels (FP8 or INT4 cache)
     if (workspace_bytes < tc::tc_workspace_bytes(num_lanes, window, num_q_heads, cache->num_kv_heads, num_sms))
       return SDVA_ERR_WORKSPACE;
     const size_t slots = (size_t)num_lanes * cache->num_kv_heads + num_sms;
     tc::TcArgs t;
     t.q = static_cast<const uint16_t*>(q);
+    t.k_codes = static_cast<const uint8_t*>(cache->k_codes);
+    t.v_codes = static_cast<const uint8_t*>(cache->v_codes);
     t.page_table = page_table;
     t.seq_lens = seq_lens;
-    t.k_scales = static_cast<const float*>(cache->k_scales);
-    t.v_scales = static_cast<const float*>(cache->v_scales);
+    t.k_scales = cache->k_scales;
+    t.v_scales = cache->v_scales;
     t.ws_ml = reinterpret_cast<float2*>(workspace);
     t.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                       (slots * plan.R * sizeof(float2) + 255) / 256 * 256);

@@ -41,6 +41,8 @@
 //     next page overlaps the rest of the softmax.
 //   * Every wait is bounded; on timeout the CTA raises SDVA_STATUS_TIMEOUT,
 //     drains its own copies and MMAs, frees tensor memory and returns.
+#include <string.h>
+
 #include "tc_primitives.cuh"
 #include "verify_attn_tc.cuh"
 
@@ -49,19 +51,28 @@ namespace tc {
 namespace {
 
 constexpr int kStages = 8;
-constexpr int kStageBytes = 16384;   // K tile + V tile of one (page, kv head)
-constexpr int kTileBytes = 8192;     // 64 rows x 128 E4M3 codes
+constexpr int kTileBytes = 8192;     // FP8: 64 rows x 128 E4M3 codes
+constexpr int kI4Codes = 4096;       // INT4: 64 rows x 64 code bytes
+constexpr int kI4Scales = 512;       // INT4: 64 rows x 4 fp16 group scales
 constexpr int kV16Stages = 4;
-constexpr int kV16Bytes = 16384;     // fp16 V of one page: dims 0-63 | dims 64-127, 64 rows x 128 B each
+constexpr int kV16Bytes = 16384;     // fp16 K or V of one page: dims 0-63 | dims 64-127, 64 rows x 128 B each
 constexpr int kProducerWarp = 8;
 constexpr int kQkWarp = 9;           // + warpgroup index
 constexpr int kPvWarp = 11;
 constexpr int kConvWarp = 12;        // converters: warps 12-15
 constexpr int kThreads = 16 * 32;
-// shared memory: the fp16 V ring first, then the K/V stages, then Ctl
-constexpr uint32_t kOffV16 = 0;
-constexpr uint32_t kOffStages = kOffV16 + kV16Stages * kV16Bytes;
-constexpr uint32_t kOffCtl = kOffStages + kStages * kStageBytes;
+// Shared memory: the fp16 V ring, the fp16 K ring (INT4 only), the K/V code
+// stages, then Ctl.  A stage holds one (page, kv head): FP8 K and V tiles
+// (TMA, 128-byte swizzle), or INT4 K codes, V codes, K scales, V scales.
+template <int KVT>
+struct Smem {
+  static constexpr bool kInt4 = KVT == SDVA_KV_INT4_G32;
+  static constexpr uint32_t kStageBytes = kInt4 ? 2 * kI4Codes + 2 * kI4Scales : 2 * kTileBytes;
+  static constexpr uint32_t kOffV16 = 0;
+  static constexpr uint32_t kOffK16 = kOffV16 + kV16Stages * kV16Bytes;
+  static constexpr uint32_t kOffStages = kOffK16 + (kInt4 ? kV16Stages * kV16Bytes : 0);
+  static constexpr uint32_t kOffCtl = kOffStages + kStages * kStageBytes;
+};
 // Register split: launched at 128 per thread (65536 for the block); the two
 // softmax warpgroups grow to kRegsSoftmax, the other two shrink to kRegsOther.
 constexpr int kRegsSoftmax = 176;
@@ -74,6 +85,7 @@ __host__ __device__ constexpr uint32_t col_p(int j) { return 192u + 32u * j; }  
 __host__ __device__ constexpr uint32_t col_o(int j) { return 256u + 128u * j; }  // 128 fp32 cols
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_e4m3(128, 64, 0);
+constexpr uint32_t kIdescQK16 = idesc_f16(128, 64, 0);
 constexpr uint32_t kIdescPV = idesc_f16(128, 128, 1);
 constexpr float kTau = 8.0f;       // allowed lag of the running max (log2 units)
 constexpr float kPScale = 128.0f;  // P' = softmax weight * 2^(15 - kTau) <= 2^15 (fp16)
@@ -85,6 +97,8 @@ struct Ctl {
   uint64_t empty[kStages];  // the stage's K was used by QK, its V converted, its scales read
   uint64_t v16_full[kV16Stages];   // fp16 V written (one arrival per converter warp)
   uint64_t v16_empty[kV16Stages];  // the PV that read it completed
+  uint64_t k16_full[kV16Stages];   // INT4: fp16 K written (one arrival per converter warp)
+  uint64_t k16_empty[kV16Stages];  // INT4: the QK that read it completed
   uint64_t s_full[2];       // QK of warpgroup j's current page is in S_j
   uint64_t s_free[2];       // warpgroup j has copied S_j to registers
   uint64_t p_full[2];       // warpgroup j wrote P_j
@@ -103,8 +117,12 @@ struct Ctl {
   int lens[kMaxLanesTc];      // L_b
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kOffCtl + sizeof(Ctl);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <int KVT>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Smem<KVT>::kOffCtl + sizeof(Ctl);
+}
+static_assert(smem_bytes<SDVA_KV_FP8_E4M3>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<SDVA_KV_INT4_G32>() <= 232448, "shared memory budget");
 
 __device__ __forceinline__ long long cta_start(long long c, long long C, long long total) { return c * total / C; }
 
@@ -196,6 +214,50 @@ __device__ __forceinline__ void split_q_half(const uint16_t* qrow, int e, int ha
   }
 }
 
+// Half `half` (dims 64 * half .. + 63) of the Q row scaled by 2^e, as fp16
+// pairs (word w = dims 64 * half + 2w, + 1).  A null row gives zeros.
+__device__ __forceinline__ void q16_half(const uint16_t* qrow, int e, int half, uint32_t (&w)[32]) {
+  const float up = ldexpf(1.0f, e);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (qrow) v = reinterpret_cast<const uint4*>(qrow)[8 * half + k];
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) w[4 * k + t] = pack_f16x2(bf16_lo(x[t]) * up, bf16_hi(x[t]) * up);
+  }
+}
+
+// 16 bytes of INT4 codes (32 dims of one key, dims 2i / 2i + 1 in the low /
+// high nibble of byte i, two's complement) times their group's fp16 scale ->
+// 32 fp16 values as 4 x 16-byte chunks (chunk k = dims 8k .. 8k + 7).  A
+// nibble u becomes the exact fp16 1024 + (u ^ 8) by bit placement; minus 1032
+// that is its signed value, then one rounding by the scale.
+__device__ __forceinline__ void int4_group_to_f16(uint4 codes, uint32_t scale_bits, uint4 (&out)[4]) {
+  const __half2 s2 = __halves2half2(__ushort_as_half((unsigned short)scale_bits),
+                                    __ushort_as_half((unsigned short)scale_bits));
+  const __half2 bias = __floats2half2_rn(1032.0f, 1032.0f);
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = cw[k] & 0x0F0F0F0Fu, hi = (cw[k] >> 4) & 0x0F0F0F0Fu;
+    const uint32_t d03 = __byte_perm(lo, hi, 0x5140);  // bytes: dims 0, 1, 2, 3 of this word
+    const uint32_t d47 = __byte_perm(lo, hi, 0x7362);  // dims 4, 5, 6, 7
+    uint32_t h[4];
+    const uint32_t src[2] = {d03, d47};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t spread = __byte_perm(src[q >> 1], 0u, (q & 1) ? 0x4342 : 0x4140);  // two dims, 16 bits each
+      const uint32_t biased = (spread | 0x64006400u) ^ 0x00080008u;
+      __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&biased), bias);
+      v = __hmul2(v, s2);
+      h[q] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    out[k] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+template <int KVT>
 __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                     const __grid_constant__ CUtensorMap map_v,
                                                                     TcArgs a) {
@@ -203,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(base_ptr + kOffCtl);
+  using SM = Smem<KVT>;
+  constexpr bool kInt4 = SM::kInt4;
+  constexpr uint32_t kStageBytes = SM::kStageBytes;
+  Ctl* ctl = reinterpret_cast<Ctl*>(base_ptr + SM::kOffCtl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = gridDim.x, c = blockIdx.x;
   volatile int* abort_flag = &ctl->abort;
@@ -236,11 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1 + 4 + row_threads / 32);  // QK commit, converters, softmax warps
+      // FP8: QK commit (K tile), converters (V tile), softmax warps (scales);
+      // INT4: converters (K and V codes), softmax warps
+      mbar_init(smem_u32(&ctl->empty[s]), (kInt4 ? 0 : 1) + 4 + row_threads / 32);
     }
     for (int t = 0; t < kV16Stages; ++t) {
       mbar_init(smem_u32(&ctl->v16_full[t]), 4);
       mbar_init(smem_u32(&ctl->v16_empty[t]), 1);
+      mbar_init(smem_u32(&ctl->k16_full[t]), 4);
+      mbar_init(smem_u32(&ctl->k16_empty[t]), 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(smem_u32(&ctl->s_full[j]), 1);
@@ -267,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
-  const uint32_t stages = base + kOffStages;
-  const uint32_t v16 = base + kOffV16;
+  const uint32_t stages = base + SM::kOffStages;
+  const uint32_t v16 = base + SM::kOffV16;
+  const uint32_t k16 = base + SM::kOffK16;
   // Each warpgroup changes its register budget as a whole, before its warps
   // take their roles.
   if (warp >= 8) {
@@ -278,37 +348,38 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     // producer: page ids and scales prefetched 32 pages at a time, two
     // batches ahead; lane 0 issues the TMA loads.
     // ------------------------------------------------------------------
-    prefetch_tmap(&map_k);
-    prefetch_tmap(&map_v);
-    auto locate = [&](long long g, int& row_coord, int& ph_out) {
-      row_coord = 0;
-      ph_out = -1;
-      if (g < n_local) {
-        PageIter it;
-        it.seek(start + g, ctl->pref, a.B, a.Hkv);
-        int pid = a.page_table[(size_t)it.b * a.max_pages + it.p];
-        if (pid < 0 || pid >= a.num_pages) pid = 0;  // the merge zeroes lanes with bad ids
-        ph_out = pid * a.Hkv + it.hk;
-        row_coord = ph_out * kPage;
-      }
+    if constexpr (!kInt4) {
+      prefetch_tmap(&map_k);
+      prefetch_tmap(&map_v);
+    }
+    // (page, kv head) index of position g of this CTA's range, -1 past its end
+    auto locate = [&](long long g) -> int {
+      if (g >= n_local) return -1;
+      PageIter it;
+      it.seek(start + g, ctl->pref, a.B, a.Hkv);
+      int pid = a.page_table[(size_t)it.b * a.max_pages + it.p];
+      if (pid < 0 || pid >= a.num_pages) pid = 0;  // the merge zeroes lanes with bad ids
+      return pid * a.Hkv + it.hk;
     };
-    int rc_a, ph_a, rc_b, ph_b;
-    locate(lane, rc_a, ph_a);
-    locate(32 + lane, rc_b, ph_b);
-    float sk_a = ph_a >= 0 ? a.k_scales[ph_a] : 0.0f;
-    float sv_a = ph_a >= 0 ? a.v_scales[ph_a] : 0.0f;
+    // the page's scale terms for the softmax (INT4 scales are applied by the converters)
+    auto k_scale_of = [&](int ph) -> float {
+      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.k_scales)[ph] : 0.0f);
+    };
+    auto v_scale_of = [&](int ph) -> float {
+      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph] : 0.0f);
+    };
+    int ph_a = locate(lane), ph_b = locate(32 + lane);
+    float sk_a = k_scale_of(ph_a), sv_a = v_scale_of(ph_a);
     long long issued = 0;
     bool ok = true;
     for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
-      int rc_c, ph_c;
-      locate(g0 + 64 + lane, rc_c, ph_c);
-      const float sk_b = ph_b >= 0 ? a.k_scales[ph_b] : 0.0f;
-      const float sv_b = ph_b >= 0 ? a.v_scales[ph_b] : 0.0f;
+      const int ph_c = locate(g0 + 64 + lane);
+      const float sk_b = k_scale_of(ph_b), sv_b = v_scale_of(ph_b);
       const float shift_a = sv_a > 0.0f ? log2f(sv_a) : 0.0f;
       const float inv_a = sv_a > 0.0f ? 1.0f / sv_a : 1.0f;
       for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
         const long long g = g0 + i;
-        const int rc = __shfl_sync(0xffffffffu, rc_a, i);
+        const int ph = __shfl_sync(0xffffffffu, ph_a, i);
         const float sk = __shfl_sync(0xffffffffu, sk_a, i);
         const float sh = __shfl_sync(0xffffffffu, shift_a, i);
         const float iv = __shfl_sync(0xffffffffu, inv_a, i);
@@ -320,17 +391,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           ctl->shift[s] = sh;
           ctl->inv_v[s] = iv;
           const uint32_t bar = smem_u32(&ctl->full[s]);
+          const uint32_t dst = stages + s * kStageBytes;
           mbar_arrive_expect_tx(bar, kStageBytes);
-          tma_load_2d(stages + s * kStageBytes, &map_k, 0, rc, bar);
-          tma_load_2d(stages + s * kStageBytes + kTileBytes, &map_v, 0, rc, bar);
+          if constexpr (kInt4) {
+            // K codes | V codes | K scales | V scales, each contiguous per (page, kv head)
+            bulk_load(dst, a.k_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
+            bulk_load(dst + kI4Codes, a.v_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
+            bulk_load(dst + 2 * kI4Codes, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * kI4Scales, kI4Scales,
+                      bar);
+            bulk_load(dst + 2 * kI4Codes + kI4Scales, static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * kI4Scales,
+                      kI4Scales, bar);
+          } else {
+            tma_load_2d(dst, &map_k, 0, ph * kPage, bar);
+            tma_load_2d(dst + kTileBytes, &map_v, 0, ph * kPage, bar);
+          }
         }
         __syncwarp();
         issued = g + 1;
       }
-      rc_a = rc_b;
+      ph_a = ph_b;
       sk_a = sk_b;
       sv_a = sv_b;
-      rc_b = rc_c;
       ph_b = ph_c;
     }
     if (!ok) {
@@ -359,21 +440,36 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (!(ok = mbar_wait(smem_u32(&ctl->q_full), q_phase, abort_flag))) break;
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
-        const int s = (int)(h % kStages);
-        if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
+        const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
+        // FP8: the page's K tile as loaded; INT4: its fp16 K from the converters
+        if (!(ok = kInt4 ? mbar_wait(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag)
+                         : mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag)))
+          break;
         if (h >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[j]), (uint32_t)(((h - 2) >> 1) & 1), abort_flag)))
           break;
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t ktile = stages + s * kStageBytes;
+          if constexpr (kInt4) {
+            // S = Q K^T, kind::f16: Q as fp16 in tensor memory (8 columns per
+            // 16 dims), K rows of 128 bytes per 64-dim half (halves 8192 apart)
+            const uint32_t kt = k16 + t * kV16Bytes;
 #pragma unroll
-          for (int half = 0; half < 2; ++half)
+            for (int k = 0; k < 8; ++k)
+              mma_f16_ts(tmem + col_s(j), tmem + kColQ + 8 * k, sdesc_sw128(kt + 8192 * (k >> 2) + 32 * (k & 3), 1024, 1024),
+                         kIdescQK16, k == 0 ? 0u : 1u);
+            mma_commit(smem_u32(&ctl->s_full[j]));
+            mma_commit(smem_u32(&ctl->k16_empty[t]));
+          } else {
+            const uint32_t ktile = stages + s * kStageBytes;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_e4m3_ts(tmem + col_s(j), tmem + kColQ + 32 * half + 8 * k, sdesc_sw128(ktile + 32 * k, 1024, 1024),
-                          kIdescQK, (half == 0 && k == 0) ? 0u : 1u);
-          mma_commit(smem_u32(&ctl->s_full[j]));
-          mma_commit(smem_u32(&ctl->empty[s]));
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_e4m3_ts(tmem + col_s(j), tmem + kColQ + 32 * half + 8 * k,
+                            sdesc_sw128(ktile + 32 * k, 1024, 1024), kIdescQK, (half == 0 && k == 0) ? 0u : 1u);
+            mma_commit(smem_u32(&ctl->s_full[j]));
+            mma_commit(smem_u32(&ctl->empty[s]));
+          }
         }
         __syncwarp();
         last = h;
@@ -456,10 +552,34 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (h >= kV16Stages &&
           !(ok = mbar_wait(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
         break;
-      const uint8_t* src = base_ptr + kOffStages + s * kStageBytes + kTileBytes;
-      uint8_t* dst = base_ptr + kOffV16 + t * kV16Bytes;
+      if (kInt4 && h >= kV16Stages &&
+          !(ok = mbar_wait(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+        break;
+      const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
+      uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
+      if constexpr (kInt4) {
+        // INT4: K and V, 64 rows x 4 groups of 32 dims each; group (tk, r, gi)
+        // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
+        // it is the K-major operand of the QK MMA)
+        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 4; ++q) {
+          const int item = u + 128 * q;  // 512 groups per page
+          const int tk = item >> 8, r = (item >> 2) & 63, gi = item & 3;
+          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * kI4Codes + r * 64 + gi * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * kI4Codes + tk * kI4Scales + r * 8 + gi * 2);
+          uint4 ch[4];
+          int4_group_to_f16(codes, sc, ch);
+          // dims 32gi .. 32gi + 31 -> region gi >> 1, 8-dim chunks 4 (gi & 1) .. + 3
+          uint8_t* reg = (tk ? dst : kdst) + (gi >> 1) * 8192 + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(reg + (((4 * (gi & 1) + k) ^ (r & 7)) << 4)) = ch[k];
+        }
+      } else {
+        const uint8_t* src = stage + kTileBytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
         const int item = u + 128 * q;
         const int r = item >> 3, c = item & 7;  // key row, 16-dim chunk
         const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
@@ -475,12 +595,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const int c0 = 2 * (c & 3);
         *reinterpret_cast<uint4*>(reg + (((c0) ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
         *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+        }
       }
       // generic-proxy writes -> visible to the tensor core
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&ctl->v16_full[t]));
+        if (kInt4) mbar_arrive(smem_u32(&ctl->k16_full[t]));
         mbar_arrive(smem_u32(&ctl->empty[s]));
       }
     }
@@ -521,10 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (ok) {
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
-            uint32_t hi[16], lo[16];
-            split_q_half(row_valid ? qrow : nullptr, e, half, hi, lo);
-            tmem_st16(lane_base + kColQ + 16 * half, hi);
-            tmem_st16(lane_base + kColQ + 32 + 16 * half, lo);
+            if constexpr (kInt4) {
+              uint32_t qw[32];
+              q16_half(row_valid ? qrow : nullptr, e, half, qw);
+              tmem_st32(lane_base + kColQ + 32 * half, qw);
+            } else {
+              uint32_t hi[16], lo[16];
+              split_q_half(row_valid ? qrow : nullptr, e, half, hi, lo);
+              tmem_st16(lane_base + kColQ + 16 * half, hi);
+              tmem_st16(lane_base + kColQ + 32 + 16 * half, lo);
+            }
             tmem_wait_st();
           }
           fence_before_sync();
@@ -807,25 +935,43 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
   const long long c_first = s_first, c_last = s_last;
   if (c_first == c_last || r >= a.R) return;  // one segment: the split kernel wrote the rows
   const int nseg = (int)(c_last - c_first + 1);
+  const size_t row0 = (size_t)(u + c_first) * a.R + r;  // segment k's partial row: row0 + k * R
   float M = -INFINITY;
-  for (int sgi = lane; sgi < nseg; sgi += 32) {
-    M = fmaxf(M, a.ws_ml[(size_t)(u + c_first + sgi) * a.R + r].x);
-  }
+  for (int sgi = lane; sgi < nseg; sgi += 32) M = fmaxf(M, a.ws_ml[row0 + (size_t)sgi * a.R].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // Segments in groups of 32: lane k holds the weight of segment s0 + k; the
+  // partial rows are read 8 at a time so their loads are in flight together.
   float den = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-  for (int sgi = 0; sgi < nseg; ++sgi) {
-    const size_t slot_row = (size_t)(u + c_first + sgi) * a.R + r;
-    const float2 ml = a.ws_ml[slot_row];
-    const float4 v = *reinterpret_cast<const float4*>(a.ws_o + slot_row * kHeadDim + lane * 4);
-    const float w = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);
-    den += w * ml.y;
-    acc[0] += w * v.x;
-    acc[1] += w * v.y;
-    acc[2] += w * v.z;
-    acc[3] += w * v.w;
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    float wk = 0.0f;
+    if (s0 + lane < nseg) {
+      const float2 ml = a.ws_ml[row0 + (size_t)(s0 + lane) * a.R];
+      wk = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);
+      den += wk * ml.y;
+    }
+    const int n = min(32, nseg - s0);
+    for (int q = 0; q < n; q += 8) {
+      float w[8];
+      float4 v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        w[t] = __shfl_sync(0xffffffffu, wk, (q + t) & 31);
+        v[t] = q + t < n ? *reinterpret_cast<const float4*>(a.ws_o + (row0 + (size_t)(s0 + q + t) * a.R) * kHeadDim +
+                                                             lane * 4)
+                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        acc[0] += w[t] * v[t].x;
+        acc[1] += w[t] * v[t].y;
+        acc[2] += w[t] * v[t].z;
+        acc[3] += w[t] * v[t].w;
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = 1.0f / den;
   const int i = r / a.G, h = hk * a.G + r % a.G;
   uint16_t* dst = a.out + (((size_t)b * a.W + i) * a.Hq + h) * kHeadDim + lane * 4;
@@ -876,16 +1022,30 @@ size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms) {
 bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms) {
   const int Hkv = cache->num_kv_heads;
   const int R = W * (Hq / Hkv);
-  return cache->dtype == SDVA_KV_FP8_E4M3 && R <= 128 && B <= kMaxLanesTc && num_sms > 0 &&
-         (long long)cache->num_pages * Hkv * kPage < (1LL << 31) && encoder() != nullptr;
+  const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || (cache->dtype == SDVA_KV_FP8_E4M3 && encoder() != nullptr);
+  return dtype_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 &&
+         (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }
 
 int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream) {
-  CUtensorMap mk, mv;
-  const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
-  if (!encode_pool_map(&mk, cache->k_codes, rows) || !encode_pool_map(&mv, cache->v_codes, rows)) return SDVA_ERR_CUDA;
-  cudaFuncSetAttribute(verify_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  verify_split_tc_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(mk, mv, args);
+  if (cache->dtype == SDVA_KV_INT4_G32) {
+    // the INT4 pools are read with 1-D bulk copies: no tensor maps
+    CUtensorMap none;
+    memset(&none, 0, sizeof(none));
+    cudaFuncSetAttribute(verify_split_tc_kernel<SDVA_KV_INT4_G32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem_bytes<SDVA_KV_INT4_G32>());
+    verify_split_tc_kernel<SDVA_KV_INT4_G32>
+        <<<num_sms, kThreads, smem_bytes<SDVA_KV_INT4_G32>(), stream>>>(none, none, args);
+  } else {
+    CUtensorMap mk, mv;
+    const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
+    if (!encode_pool_map(&mk, cache->k_codes, rows) || !encode_pool_map(&mv, cache->v_codes, rows))
+      return SDVA_ERR_CUDA;
+    cudaFuncSetAttribute(verify_split_tc_kernel<SDVA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem_bytes<SDVA_KV_FP8_E4M3>());
+    verify_split_tc_kernel<SDVA_KV_FP8_E4M3>
+        <<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
+  }
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(args.B * args.Hkv, (args.R + 7) / 8, 1);

@@ -14,11 +14,13 @@ namespace tc {
 constexpr int kMaxLanesTc = 1024;  // lanes per call handled by the tcgen05 path
 
 struct TcArgs {
-  const uint16_t* q;  // bf16 [B][W][Hq][128]
+  const uint16_t* q;        // bf16 [B][W][Hq][128]
+  const uint8_t* k_codes;   // INT4 pools (the FP8 pools are read through tensor maps)
+  const uint8_t* v_codes;
   const int32_t* page_table;
   const int32_t* seq_lens;
-  const float* k_scales;  // [pages][Hkv]
-  const float* v_scales;
+  const void* k_scales;  // FP8: f32 [pages][Hkv]; INT4: f16 [pages][Hkv][64][4]
+  const void* v_scales;
   float2* ws_ml;  // [lanes * Hkv + ctas][R]
   float* ws_o;    // [lanes * Hkv + ctas][R][128]
   uint16_t* out;  // bf16 [B][W][Hq][128]
@@ -29,7 +31,7 @@ struct TcArgs {
 
 // Scratch bytes of the tcgen05 path (split-K partials, one slot per unit and per CTA).
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms);
-// Whether the tcgen05 path handles this call (FP8 cache, <= 128 rows per kv head, ...).
+// Whether the tcgen05 path handles this call (<= 128 rows per kv head, ...).
 bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms);
 // Enqueue the split and merge kernels on `stream`.
 int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream);
