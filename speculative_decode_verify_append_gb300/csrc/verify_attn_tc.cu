@@ -89,6 +89,7 @@ constexpr uint32_t kIdescQK16 = idesc_f16(128, 64, 0);
 constexpr uint32_t kIdescPV = idesc_f16(128, 128, 1);
 constexpr float kTau = 8.0f;       // allowed lag of the running max (log2 units)
 constexpr float kPScale = 128.0f;  // P' = softmax weight * 2^(15 - kTau) <= 2^15 (fp16)
+constexpr int kBadPage = 1 << 30;  // marks a page whose id was out of range (bit free in a (page, head) index)
 constexpr int kBarWg1Done = 1;    // named barriers between the two softmax warpgroups
 constexpr int kBarWg0Done = 2;
 
@@ -106,6 +107,8 @@ struct Ctl {
   uint64_t q_full;          // warpgroup 0 wrote the segment's Q
   uint64_t q_free;          // both QK issuers are done with the segment (2 arrivals)
   float sk[kStages];        // K scale of the page in stage s
+  int bad[kStages];         // the page id in stage s was out of range (page 0 was loaded instead)
+  int bad1;                 // warpgroup 1 met such a page in the current segment
   float shift[kStages];     // log2 of its V scale (0 when the scale is 0)
   float inv_v[kStages];     // 1 / V scale (1 when the scale is 0)
   float m1[128];            // warpgroup 1's running max / sum at the end of a segment
@@ -352,21 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       prefetch_tmap(&map_k);
       prefetch_tmap(&map_v);
     }
-    // (page, kv head) index of position g of this CTA's range, -1 past its end
+    // (page, kv head) index of position g of this CTA's range, -1 past its
+    // end; an out-of-range page id loads page 0 instead and is marked with
+    // kBadPage (the lane's rows are then written as zeros and flagged)
     auto locate = [&](long long g) -> int {
       if (g >= n_local) return -1;
       PageIter it;
       it.seek(start + g, ctl->pref, a.B, a.Hkv);
-      int pid = a.page_table[(size_t)it.b * a.max_pages + it.p];
-      if (pid < 0 || pid >= a.num_pages) pid = 0;  // the merge zeroes lanes with bad ids
+      const int pid = a.page_table[(size_t)it.b * a.max_pages + it.p];
+      if (pid < 0 || pid >= a.num_pages) return it.hk | kBadPage;
       return pid * a.Hkv + it.hk;
     };
     // the page's scale terms for the softmax (INT4 scales are applied by the converters)
     auto k_scale_of = [&](int ph) -> float {
-      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.k_scales)[ph] : 0.0f);
+      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.k_scales)[ph & ~kBadPage] : 0.0f);
     };
     auto v_scale_of = [&](int ph) -> float {
-      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph] : 0.0f);
+      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph & ~kBadPage] : 0.0f);
     };
     int ph_a = locate(lane), ph_b = locate(32 + lane);
     float sk_a = k_scale_of(ph_a), sv_a = v_scale_of(ph_a);
@@ -379,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       const float inv_a = sv_a > 0.0f ? 1.0f / sv_a : 1.0f;
       for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
         const long long g = g0 + i;
-        const int ph = __shfl_sync(0xffffffffu, ph_a, i);
+        const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
+        const int ph = ph_m & ~kBadPage;
         const float sk = __shfl_sync(0xffffffffu, sk_a, i);
         const float sh = __shfl_sync(0xffffffffu, shift_a, i);
         const float iv = __shfl_sync(0xffffffffu, inv_a, i);
@@ -387,6 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (g >= kStages && !(ok = mbar_wait(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
           break;
         if (lane == 0) {
+          const int page_bad = (ph_m & kBadPage) ? 1 : 0;
+          if (page_bad) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
+          ctl->bad[s] = page_bad;
           ctl->sk[s] = sk;
           ctl->shift[s] = sh;
           ctl->inv_v[s] = iv;
@@ -664,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
 
       float m = -INFINITY, l = 0.0f;
       bool had_page = false;
+      int seg_bad = 0;
       for (long long k = 0; k < seg_len && ok; ++k, ++g) {
         if ((int)(g & 1) != wg) continue;
         had_page = true;
@@ -676,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
         fence_after_sync();
         const float kscale = ctl->sk[s] * row_scale, shift = ctl->shift[s], inv_f = ctl->inv_v[s];
+        seg_bad |= ctl->bad[s];
         // the stage's scale terms are in registers: this warp's share of releasing the stage
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
@@ -783,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (wg == 1) {
         ctl->m1[row] = (had_page && warp_active) ? m : -INFINITY;
         ctl->l1[row] = (had_page && warp_active) ? l : 0.0f;
+        if (row == 0) ctl->bad1 = seg_bad;
         named_arrive(kBarWg1Done, 256);
         named_sync(kBarWg0Done, 256);  // warpgroup 0 has read this warpgroup's O
         fence_after_sync();
@@ -794,7 +806,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       const bool stop = !ok || *abort_flag;
       const bool had0 = seg_len > 1 || (g_first & 1) == 0;  // warpgroup 0 owned a page of this segment
       const bool had1 = seg_len > 1 || (g_first & 1) == 1;  // warpgroup 1 owned a page of this segment
-      if (warp_active && !stop) {
+      // a page id out of range anywhere in the segment: zero rows for a whole
+      // unit, a NaN max marks the partial for the merge
+      const bool bad = (seg_bad | ctl->bad1) != 0;
+      if (warp_active && !stop && bad && row_valid) {
+        if (whole_unit) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim);
+#pragma unroll 4
+          for (int t = 0; t < 16; ++t) dst[t] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          a.ws_ml[((size_t)(u + c)) * a.R + row] = make_float2(__int_as_float(0x7fc00000), 0.0f);
+        }
+      }
+      if (warp_active && !stop && !bad) {
         const float m0 = had0 ? m : -INFINITY, l0 = had0 ? l : 0.0f;
         const float mm1 = ctl->m1[row], ll1 = ctl->l1[row];
         const float M = fmaxf(m0, mm1);
@@ -865,31 +889,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   }
 }
 
-// grid: (units, ceil(R / 8)); block 256 = one warp per row.  Zeroes the rows
-// of invalid lanes (and flags them); merges the partials of units that span
-// several CTAs by log-sum-exp.
-__global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
-  const int u = blockIdx.x;
-  const int b = u / a.Hkv, hk = u % a.Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ int s_bad;
-  __shared__ long long s_first, s_last;
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
+// Merge prologue, run by warp 0 of a block: whether lane b's length fits, and
+// the first and last CTA whose page range holds part of unit (b, hk) (same
+// partition rule as the split kernel).
+__device__ __forceinline__ bool merge_locate(const TcArgs& a, int C, int b, int hk, int warp, int lane,
+                                             long long* s_first, long long* s_last) {
   const int L = a.seq_lens[b];
   const bool len_ok = L >= 0 && L <= a.max_context && (long long)L + a.W <= (long long)a.max_pages * kPage;
   const int nb = len_ok ? (L + a.W + kPage - 1) / kPage : 0;
-  if (!len_ok) {
-    if (threadIdx.x == 0) s_bad = SDVA_STATUS_OVERFLOW;
-  } else {
-    const int32_t* prow = a.page_table + (size_t)b * a.max_pages;
-    for (int p = threadIdx.x; p < nb; p += blockDim.x) {
-      const int id = prow[p];
-      if (id < 0 || id >= a.num_pages) s_bad = SDVA_STATUS_BAD_PAGE;
-    }
-  }
   if (warp == 0) {
-    // pages before this lane and in total (same rule as the split kernel)
     long long before = 0, all = 0;
     for (int bb = lane; bb < a.B; bb += 32) {
       const int Lb = a.seq_lens[bb];
@@ -913,33 +921,55 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
         while (cc > 0 && cta_start(cc, Ce, total) > x) --cc;
         return cc;
       };
-      s_first = locate(Pu);
-      s_last = locate(Pu + nb - 1);
+      *s_first = locate(Pu);
+      *s_last = locate(Pu + nb - 1);
     }
   }
+  return len_ok;
+}
+
+// grid: (units, ceil(R / 8)); block 256 = one warp per row, for units that
+// span few CTAs.  Same duties as verify_merge_tc_kernel below.
+__global__ void __launch_bounds__(256) verify_merge_rows_tc_kernel(TcArgs a, int C) {
+  const int u = blockIdx.x;
+  const int b = u / a.Hkv, hk = u % a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ long long s_first, s_last;
+  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, &s_first, &s_last);
   __syncthreads();
-  // launched as a programmatic dependent of the split kernel: everything
-  // above overlapped its tail; its partials and rows are visible after this
+  // programmatic dependent of the split kernel (see verify_merge_tc_kernel)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int bad = s_bad;
   const int r = blockIdx.y * 8 + warp;
-  if (bad) {
-    if (threadIdx.x == 0 && blockIdx.y == 0 && hk == 0) raise_status(a.status, bad);
-    if (r < a.R) {
-      const int i = r / a.G, h = hk * a.G + r % a.G;
-      uint16_t* dst = a.out + (((size_t)b * a.W + i) * a.Hq + h) * kHeadDim + lane * 4;
-      *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
-    }
+  if (r >= a.R) return;
+  const int i = r / a.G, h = hk * a.G + r % a.G;
+  uint16_t* dst = a.out + (((size_t)b * a.W + i) * a.Hq + h) * kHeadDim + lane * 4;
+  if (!len_ok) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+    if (lane == 0 && r == 0 && hk == 0) raise_status(a.status, SDVA_STATUS_OVERFLOW);
     return;
   }
   const long long c_first = s_first, c_last = s_last;
-  if (c_first == c_last || r >= a.R) return;  // one segment: the split kernel wrote the rows
+  if (c_first == c_last) return;  // one segment: the split kernel wrote the row
   const int nseg = (int)(c_last - c_first + 1);
   const size_t row0 = (size_t)(u + c_first) * a.R + r;  // segment k's partial row: row0 + k * R
   float M = -INFINITY;
-  for (int sgi = lane; sgi < nseg; sgi += 32) M = fmaxf(M, a.ws_ml[row0 + (size_t)sgi * a.R].x);
+  int bad = 0;
+  for (int k = lane; k < nseg; k += 32) {
+    const float mk = a.ws_ml[row0 + (size_t)k * a.R].x;
+    if (isnan(mk))
+      bad = 1;
+    else
+      M = fmaxf(M, mk);
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  if (bad) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+    return;
+  }
   // Segments in groups of 32: lane k holds the weight of segment s0 + k; the
   // partial rows are read 8 at a time so their loads are in flight together.
   float den = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -973,10 +1003,107 @@ __global__ void __launch_bounds__(256) verify_merge_tc_kernel(TcArgs a, int C) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = 1.0f / den;
-  const int i = r / a.G, h = hk * a.G + r % a.G;
-  uint16_t* dst = a.out + (((size_t)b * a.W + i) * a.Hq + h) * kHeadDim + lane * 4;
   *reinterpret_cast<uint2*>(dst) =
       make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+}
+
+// grid: (units, R); block 256 = 8 warps on one row, for units that span
+// many CTAs (the warps divide the unit's segments).  Zeroes the rows of
+// lanes whose length does not fit (and flags them) and of units whose split
+// met an out-of-range page id (the split flagged those); merges by
+// log-sum-exp the partials of units that span several CTAs.
+constexpr int kMergeThreads = 256;
+constexpr int kMaxSegments = 1024;  // >= CTAs of the split kernel (one per SM)
+
+__global__ void __launch_bounds__(kMergeThreads) verify_merge_tc_kernel(TcArgs a, int C) {
+  const int u = blockIdx.x, r = blockIdx.y;
+  const int b = u / a.Hkv, hk = u % a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ long long s_first, s_last;
+  __shared__ float2 s_ml[kMaxSegments];
+  __shared__ float s_M, s_inv;
+  __shared__ int s_bad;
+  __shared__ float4 s_acc[kMergeThreads / 32][32];
+  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, &s_first, &s_last);
+  __syncthreads();
+  // launched as a programmatic dependent of the split kernel: everything
+  // above overlapped its tail; its partials and rows are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int i = r / a.G, h = hk * a.G + r % a.G;
+  uint16_t* dst = a.out + (((size_t)b * a.W + i) * a.Hq + h) * kHeadDim;
+  if (!len_ok) {
+    if (threadIdx.x < 32) *reinterpret_cast<uint2*>(dst + 4 * threadIdx.x) = make_uint2(0u, 0u);
+    if (threadIdx.x == 0 && r == 0 && hk == 0) raise_status(a.status, SDVA_STATUS_OVERFLOW);
+    return;
+  }
+  const long long c_first = s_first, c_last = s_last;
+  if (c_first == c_last) return;  // one segment: the split kernel wrote the row
+  const int nseg = (int)(c_last - c_first + 1);
+  const size_t row0 = (size_t)(u + c_first) * a.R + r;  // segment k's partial row: row0 + k * R
+  for (int k = threadIdx.x; k < nseg; k += kMergeThreads) s_ml[k] = a.ws_ml[row0 + (size_t)k * a.R];
+  __syncthreads();
+  if (warp == 0) {
+    float M = -INFINITY;
+    int bad = 0;
+    for (int k = lane; k < nseg; k += 32) {
+      const float mk = s_ml[k].x;
+      if (isnan(mk))
+        bad = 1;
+      else
+        M = fmaxf(M, mk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    float den = 0.0f;
+    for (int k = lane; k < nseg; k += 32) {
+      const float2 ml = s_ml[k];
+      if (ml.x != -INFINITY) den += exp2f(ml.x - M) * ml.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0) {
+      s_M = M;
+      s_bad = bad;
+      s_inv = 1.0f / den;
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x < 32) *reinterpret_cast<uint2*>(dst + 4 * threadIdx.x) = make_uint2(0u, 0u);
+    return;
+  }
+  // warp w: segments w, w + 8, ...; lane: dims 4 lane .. 4 lane + 3
+  const float M = s_M;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+  for (int k = warp; k < nseg; k += kMergeThreads / 32) {
+    const float2 ml = s_ml[k];
+    const float w = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);
+    const float4 v = *reinterpret_cast<const float4*>(a.ws_o + (row0 + (size_t)k * a.R) * kHeadDim + lane * 4);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  s_acc[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = s_acc[0][lane];
+#pragma unroll
+    for (int w2 = 1; w2 < kMergeThreads / 32; ++w2) {
+      const float4 q = s_acc[w2][lane];
+      t.x += q.x;
+      t.y += q.y;
+      t.z += q.z;
+      t.w += q.w;
+    }
+    const float inv = s_inv;
+    *reinterpret_cast<uint2*>(dst + lane * 4) =
+        make_uint2(pack_bf16x2(t.x * inv, t.y * inv), pack_bf16x2(t.z * inv, t.w * inv));
+  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1023,7 +1150,7 @@ bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms)
   const int Hkv = cache->num_kv_heads;
   const int R = W * (Hq / Hkv);
   const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || (cache->dtype == SDVA_KV_FP8_E4M3 && encoder() != nullptr);
-  return dtype_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 &&
+  return dtype_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 && num_sms <= kMaxSegments &&
          (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }
 
@@ -1047,16 +1174,21 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
         <<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
   }
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
+  // A unit spans about num_sms / units + 1 CTAs: few -> one warp per row, many
+  // -> one block of 8 warps per row.
+  const bool many = (long long)args.B * args.Hkv * 8 < (long long)num_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(args.B * args.Hkv, (args.R + 7) / 8, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = many ? dim3(args.B * args.Hkv, args.R, 1) : dim3(args.B * args.Hkv, (args.R + 7) / 8, 1);
+  cfg.blockDim = dim3(many ? kMergeThreads : 256, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, verify_merge_tc_kernel, args, num_sms) != cudaSuccess) return SDVA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, many ? verify_merge_tc_kernel : verify_merge_rows_tc_kernel, args, num_sms) !=
+      cudaSuccess)
+    return SDVA_ERR_CUDA;
   return SDVA_OK;
 }
 

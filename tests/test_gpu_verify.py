@@ -110,10 +110,13 @@ def test_split_count_changes_only_rounding():
     assert np.abs(a - b).max() <= 2 * 2.0 ** -8 * np.abs(want).max()
 
 
-def test_invalid_lanes_are_zero_and_flagged():
+@pytest.mark.parametrize("lanes", [3, 12], ids=["few-units", "many-units"])
+def test_invalid_lanes_are_zero_and_flagged(lanes):
+    """3 lanes x 2 kv heads: units span many CTAs (one merge block per row);
+    12 lanes x 2 kv heads: few CTAs per unit (one merge warp per row)."""
     sdva = _sdva()
-    lens, W = [300, 300, 300], 4
-    spec = synth.Spec("e", 6, 3, 0, 0, 8, 2, W, synth.KV_FP8, None, 0.7, True)
+    lens, W = [300] * lanes, 4
+    spec = synth.Spec("e", 6, lanes, 0, 0, 8, 2, W, synth.KV_FP8, None, 0.7, True)
     step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
     g, _, _ = fill_both(spec, step, with_oracle=False)
     table = step.page_table.copy()
