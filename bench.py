@@ -47,7 +47,7 @@ DEFAULT_WORKLOAD = "multi_lane"
 # dram bytes (read + write) of one verify_attn call (split + merge kernels),
 # measured by ncu for the current kernels, per workload (absent: not captured
 # for this workload, reported as null).  Source: profiles/verify_split_tc_fp8_multi_lane.md
-NCU_TRAFFIC_BYTES = {"multi_lane": 305_199_000 + 652_000 + 9_187_000}
+NCU_TRAFFIC_BYTES: dict = {}
 
 
 def workload_desc(spec: synth.Spec) -> str:

@@ -54,7 +54,8 @@ constexpr int kStages = 8;
 constexpr int kTileBytes = 8192;     // FP8: 64 rows x 128 E4M3 codes
 constexpr int kI4Codes = 4096;       // INT4: 64 rows x 64 code bytes
 constexpr int kI4Scales = 512;       // INT4: 64 rows x 4 fp16 group scales
-constexpr int kV16Stages = 4;
+constexpr int kV16Stages = 3;
+constexpr int kQBytes = 32768;       // Q operand: FP8 Q_hi | Q_lo (128 rows x 128 B each), or fp16 (dims 0-63 | 64-127)
 constexpr int kV16Bytes = 16384;     // fp16 K or V of one page: dims 0-63 | dims 64-127, 64 rows x 128 B each
 constexpr int kProducerWarp = 8;
 constexpr int kQkWarp = 9;           // + warpgroup index
@@ -70,7 +71,8 @@ struct Smem {
   static constexpr uint32_t kStageBytes = kInt4 ? 2 * kI4Codes + 2 * kI4Scales : 2 * kTileBytes;
   static constexpr uint32_t kOffV16 = 0;
   static constexpr uint32_t kOffK16 = kOffV16 + kV16Stages * kV16Bytes;
-  static constexpr uint32_t kOffStages = kOffK16 + (kInt4 ? kV16Stages * kV16Bytes : 0);
+  static constexpr uint32_t kOffQ = kOffK16 + (kInt4 ? kV16Stages * kV16Bytes : 0);
+  static constexpr uint32_t kOffStages = kOffQ + kQBytes;
   static constexpr uint32_t kOffCtl = kOffStages + kStages * kStageBytes;
 };
 // Register split: launched at 128 per thread (65536 for the block); the two
@@ -79,9 +81,10 @@ constexpr int kRegsSoftmax = 176;
 constexpr int kRegsOther = 80;
 static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther <= kThreads * 128, "register split");
 // tensor memory columns
-constexpr uint32_t kColQ = 0;  // Q hi: 32 cols, Q lo: 32 cols
-__host__ __device__ constexpr uint32_t col_s(int j) { return 64u + 64u * j; }    // 64 fp32 cols
-__host__ __device__ constexpr uint32_t col_p(int j) { return 192u + 32u * j; }   // hi 16 + lo 16 cols
+// S buffer x of warpgroup j: 64 fp32 columns of scores; once they are in
+// registers the warpgroup writes its P (64 keys of fp16 = 32 columns) over
+// the buffer's first half, where the PV MMA reads it
+__host__ __device__ constexpr uint32_t col_s(int j, int x) { return 128u * j + 64u * x; }
 __host__ __device__ constexpr uint32_t col_o(int j) { return 256u + 128u * j; }  // 128 fp32 cols
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_e4m3(128, 64, 0);
@@ -100,10 +103,9 @@ struct Ctl {
   uint64_t v16_empty[kV16Stages];  // the PV that read it completed
   uint64_t k16_full[kV16Stages];   // INT4: fp16 K written (one arrival per converter warp)
   uint64_t k16_empty[kV16Stages];  // INT4: the QK that read it completed
-  uint64_t s_full[2];       // QK of warpgroup j's current page is in S_j
-  uint64_t s_free[2];       // warpgroup j has copied S_j to registers
-  uint64_t p_full[2];       // warpgroup j wrote P_j
-  uint64_t pv_done[2];      // the PV that read P_j has completed
+  uint64_t s_full[2][2];    // [warpgroup j][buffer x]: QK of the buffer's page is in it
+  uint64_t p_full[2][2];    // the warpgroup wrote P over the buffer
+  uint64_t pv_done[2][2];   // the PV that read that P has completed (the buffer is free)
   uint64_t q_full;          // warpgroup 0 wrote the segment's Q
   uint64_t q_free;          // both QK issuers are done with the segment (2 arrivals)
   float sk[kStages];        // K scale of the page in stage s
@@ -193,41 +195,52 @@ __device__ __forceinline__ int q_row_exponent(const uint16_t* qrow) {
   return max(-100, min(100, 8 - k2));
 }
 
-// Half `half` (dims 64 * half .. + 63) of the Q row scaled by 2^e, split into
-// hi + lo E4M3 codes, packed 4 per word (word w = dims 64 * half + 4w .. + 3,
-// lowest byte first).  A null row gives zeros.
-__device__ __forceinline__ void split_q_half(const uint16_t* qrow, int e, int half, uint32_t (&hi)[16],
-                                             uint32_t (&lo)[16]) {
+// The Q row scaled by 2^e, split into hi + lo E4M3 codes and stored to row
+// `row` of the two shared-memory operand tiles (128-byte swizzle: 16-byte
+// chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row stores zeros.
+__device__ __forceinline__ void store_q_row_smem(const uint16_t* qrow, int e, uint8_t* qhi, uint8_t* qlo, int row) {
   const float up = ldexpf(1.0f, e);
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
+    uint32_t hw[4], lw[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (qrow) v = reinterpret_cast<const uint4*>(qrow)[8 * half + k];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int k = 0; k < 2; ++k) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qrow) v = reinterpret_cast<const uint4*>(qrow)[c * 2 + k];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int t = 0; t < 4; t += 2) {
-      const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
-      const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
-      const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
-      const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
-      const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y), l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
-      hi[2 * k + (t >> 1)] = h01 | (h23 << 16);
-      lo[2 * k + (t >> 1)] = l01 | (l23 << 16);
+      for (int t = 0; t < 4; t += 2) {
+        const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
+        const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
+        const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+        const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
+        const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y), l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
+        hw[2 * k + (t >> 1)] = h01 | (h23 << 16);
+        lw[2 * k + (t >> 1)] = l01 | (l23 << 16);
+      }
     }
+    const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }
 
-// Half `half` (dims 64 * half .. + 63) of the Q row scaled by 2^e, as fp16
-// pairs (word w = dims 64 * half + 2w, + 1).  A null row gives zeros.
-__device__ __forceinline__ void q16_half(const uint16_t* qrow, int e, int half, uint32_t (&w)[32]) {
+// The Q row scaled by 2^e as fp16, stored to row `row` of the two 64-dim
+// halves of the shared-memory operand (16384 bytes apart; 128-byte swizzle:
+// 8-dim chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row
+// stores zeros.
+__device__ __forceinline__ void store_q16_row_smem(const uint16_t* qrow, int e, uint8_t* q, int row) {
   const float up = ldexpf(1.0f, e);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
+#pragma unroll 1
+  for (int c = 0; c < 16; ++c) {  // 8 dims per 16-byte chunk
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (qrow) v = reinterpret_cast<const uint4*>(qrow)[8 * half + k];
-    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+    if (qrow) v = reinterpret_cast<const uint4*>(qrow)[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) w[4 * k + t] = pack_f16x2(bf16_lo(x[t]) * up, bf16_hi(x[t]) * up);
+    for (int t = 0; t < 4; ++t) h[t] = pack_f16x2(bf16_lo(w[t]) * up, bf16_hi(w[t]) * up);
+    const uint32_t off = 16384u * (uint32_t)(c >> 3) + (uint32_t)row * 128u + ((uint32_t)((c & 7) ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(q + off) = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
@@ -314,12 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       mbar_init(smem_u32(&ctl->k16_full[t]), 4);
       mbar_init(smem_u32(&ctl->k16_empty[t]), 1);
     }
-    for (int j = 0; j < 2; ++j) {
-      mbar_init(smem_u32(&ctl->s_full[j]), 1);
-      mbar_init(smem_u32(&ctl->s_free[j]), row_threads);
-      mbar_init(smem_u32(&ctl->p_full[j]), row_threads);
-      mbar_init(smem_u32(&ctl->pv_done[j]), 1);
-    }
+    for (int j = 0; j < 2; ++j)
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(smem_u32(&ctl->s_full[j][x]), 1);
+        mbar_init(smem_u32(&ctl->p_full[j][x]), row_threads);
+        mbar_init(smem_u32(&ctl->pv_done[j][x]), 1);
+      }
     mbar_init(smem_u32(&ctl->q_full), row_threads);
     mbar_init(smem_u32(&ctl->q_free), 2);
     ctl->abort = 0;
@@ -342,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const uint32_t stages = base + SM::kOffStages;
   const uint32_t v16 = base + SM::kOffV16;
   const uint32_t k16 = base + SM::kOffK16;
+  const uint32_t qsm = base + SM::kOffQ;
   // Each warpgroup changes its register budget as a whole, before its warps
   // take their roles.
   if (warp >= 8) {
@@ -433,9 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     }
   } else if (warp == kQkWarp || warp == kQkWarp + 1) {
     // ------------------------------------------------------------------
-    // QK issuer of warpgroup j: S_j = Q K^T for the warpgroup's pages, each
-    // as soon as its K tile has landed and the warpgroup has copied out the
-    // scores of its previous page.
+    // QK issuer of warpgroup j: S = Q K^T for the warpgroup's pages into its
+    // two S buffers in turn, each as soon as the page's K has landed and the
+    // PV that read the buffer's previous P (two own pages back) has completed.
     // ------------------------------------------------------------------
     const int j = warp - kQkWarp;
     PageIter it;
@@ -454,29 +468,34 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (!(ok = kInt4 ? mbar_wait(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag)
                          : mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag)))
           break;
-        if (h >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[j]), (uint32_t)(((h - 2) >> 1) & 1), abort_flag)))
+        const long long n = h >> 1;  // the warpgroup's own page index
+        const int x = (int)(n & 1);
+        if (n >= 2 &&
+            !(ok = mbar_wait(smem_u32(&ctl->pv_done[j][x]), (uint32_t)(((n >> 1) - 1) & 1), abort_flag)))
           break;
         fence_after_sync();
         if (lane == 0) {
+          const uint32_t d = tmem + col_s(j, x);
           if constexpr (kInt4) {
-            // S = Q K^T, kind::f16: Q as fp16 in tensor memory (8 columns per
-            // 16 dims), K rows of 128 bytes per 64-dim half (halves 8192 apart)
+            // kind::f16: Q and K as fp16 rows of 128 bytes per 64-dim half
+            // (Q halves 16384 bytes apart, K halves 8192)
             const uint32_t kt = k16 + t * kV16Bytes;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_f16_ts(tmem + col_s(j), tmem + kColQ + 8 * k, sdesc_sw128(kt + 8192 * (k >> 2) + 32 * (k & 3), 1024, 1024),
-                         kIdescQK16, k == 0 ? 0u : 1u);
-            mma_commit(smem_u32(&ctl->s_full[j]));
+              mma_f16_ss(d, sdesc_sw128(qsm + 16384 * (k >> 2) + 32 * (k & 3), 1024, 1024),
+                         sdesc_sw128(kt + 8192 * (k >> 2) + 32 * (k & 3), 1024, 1024), kIdescQK16, k == 0 ? 0u : 1u);
+            mma_commit(smem_u32(&ctl->s_full[j][x]));
             mma_commit(smem_u32(&ctl->k16_empty[t]));
           } else {
+            // kind::f8f6f4: Q_hi and Q_lo (16384 bytes apart) against the K tile as loaded
             const uint32_t ktile = stages + s * kStageBytes;
 #pragma unroll
             for (int half = 0; half < 2; ++half)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_e4m3_ts(tmem + col_s(j), tmem + kColQ + 32 * half + 8 * k,
+                mma_e4m3_ss(d, sdesc_sw128(qsm + 16384 * half + 32 * k, 1024, 1024),
                             sdesc_sw128(ktile + 32 * k, 1024, 1024), kIdescQK, (half == 0 && k == 0) ? 0u : 1u);
-            mma_commit(smem_u32(&ctl->s_full[j]));
+            mma_commit(smem_u32(&ctl->s_full[j][x]));
             mma_commit(smem_u32(&ctl->empty[s]));
           }
         }
@@ -484,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         last = h;
       }
       if (!ok) break;
-      // every QK of this segment is issued: warpgroup 0 may load the next Q
+      // every QK of this segment is issued: warpgroup 0 may store the next Q
       // once the other issuer is done too (and the softmax has consumed S)
       if (lane == 0) mbar_arrive(smem_u32(&ctl->q_free));
       __syncwarp();
@@ -496,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       // let the tensor core finish what this thread issued before tensor memory is freed
       if (last >= 0) {
         int dummy = 0;
-        mbar_wait(smem_u32(&ctl->s_full[j]), (uint32_t)((last >> 1) & 1), &dummy, 400000000LL);
+        const long long n = last >> 1;
+        mbar_wait(smem_u32(&ctl->s_full[j][n & 1]), (uint32_t)((n >> 1) & 1), &dummy, 400000000LL);
       }
     }
   } else if (warp == kPvWarp) {
@@ -514,8 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       bool fresh0 = true, fresh1 = true;
       for (long long h = g; h < g + seg_len; ++h) {
         const int j = (int)(h & 1), t = (int)(h % kV16Stages);
+        const long long n = h >> 1;  // the page's index among its warpgroup's pages
+        const int x = (int)(n & 1);
         const bool fresh = j ? fresh1 : fresh0;
-        if (!(ok = mbar_wait(smem_u32(&ctl->p_full[j]), (uint32_t)((h >> 1) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
         if (!(ok = mbar_wait(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag))) break;
         fence_after_sync();
         if (lane == 0) {
@@ -525,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           // groups 1024 bytes apart (stride byte offset)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16_ts(tmem + col_o(j), tmem + col_p(j) + 8 * k, sdesc_sw128(vt + 2048 * k, 8192, 1024), kIdescPV,
+            mma_f16_ts(tmem + col_o(j), tmem + col_s(j, x) + 8 * k, sdesc_sw128(vt + 2048 * k, 8192, 1024), kIdescPV,
                        (fresh && k == 0) ? 0u : 1u);
-          mma_commit(smem_u32(&ctl->pv_done[j]));
+          mma_commit(smem_u32(&ctl->pv_done[j][x]));
           mma_commit(smem_u32(&ctl->v16_empty[t]));
         }
         __syncwarp();
@@ -650,21 +672,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         // segment-end handshake, complete): Q may be overwritten
         if (seg_count > 0) ok = mbar_wait(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag);
         if (ok) {
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            if constexpr (kInt4) {
-              uint32_t qw[32];
-              q16_half(row_valid ? qrow : nullptr, e, half, qw);
-              tmem_st32(lane_base + kColQ + 32 * half, qw);
-            } else {
-              uint32_t hi[16], lo[16];
-              split_q_half(row_valid ? qrow : nullptr, e, half, hi, lo);
-              tmem_st16(lane_base + kColQ + 16 * half, hi);
-              tmem_st16(lane_base + kColQ + 32 + 16 * half, lo);
-            }
-            tmem_wait_st();
-          }
-          fence_before_sync();
+          // Q into the shared-memory A operand of the QK MMAs
+          uint8_t* qb = base_ptr + SM::kOffQ;
+          if constexpr (kInt4)
+            store_q16_row_smem(row_valid ? qrow : nullptr, e, qb, row);
+          else
+            store_q_row_smem(row_valid ? qrow : nullptr, e, qb, qb + 16384, row);
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
           mbar_arrive(smem_u32(&ctl->q_full));
         }
       }
@@ -681,7 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const int j = wg;
         const int p = p0 + (int)k;
         const int s = (int)(g % kStages);
-        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[j]), (uint32_t)((g >> 1) & 1), abort_flag))) break;
+        const long long n = g >> 1;  // this warpgroup's own page index
+        const int xb = (int)(n & 1);  // its S buffer
+        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
         // the producer staged the page's scale terms before completing full[s]
         if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
         fence_after_sync();
@@ -691,12 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
         uint32_t x[64];
-        tmem_ld32(lane_base + col_s(j), *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        tmem_ld32(lane_base + col_s(j) + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        tmem_ld32(lane_base + col_s(j, xb), *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(lane_base + col_s(j, xb) + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
-        // S_j is in registers: the issuer may compute the warpgroup's next page into it
-        fence_before_sync();
-        mbar_arrive(smem_u32(&ctl->s_free[j]));
         const int kbase = p * kPage;
         const int lim = L + i_row;  // last visible key position of this row
         const bool partial = kbase + kPage - 1 > lim;
@@ -717,14 +730,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
             if (kbase + q <= lim) smax = fmaxf(smax, __uint_as_float(x[q]));
         }
         const float xmax = smax == -INFINITY ? -INFINITY : fmaf(smax, kscale, shift);
-        // P_j and O_j: the PV of the warpgroup's previous page must be done
-        if (g >= 2 && !(ok = mbar_wait(smem_u32(&ctl->pv_done[j]), (uint32_t)(((g - 2) >> 1) & 1), abort_flag)))
-          break;
         // The running max may lag the true one by up to kTau (log2 units):
         // weights then reach 2^kTau and P' = w * 2^(15 - kTau) stays <= 2^15,
         // inside fp16.  O is rescaled only when some row of the warp outgrows that.
         const bool need = m != -INFINITY && xmax > m + kTau;
         if (__any_sync(0xffffffffu, need)) {
+          // O_j: the PV of the warpgroup's previous page (the latest issued)
+          // must have completed
+          if (n >= 1 && !(ok = mbar_wait(smem_u32(&ctl->pv_done[j][xb ^ 1]), (uint32_t)(((n - 1) >> 1) & 1),
+                                         abort_flag)))
+            break;
           fence_after_sync();
           const float m_new = m == -INFINITY ? m : fmaxf(m, xmax);
           const float alpha = (m == -INFINITY || m_new == m) ? 1.0f : fast_exp2(m - m_new);
@@ -772,12 +787,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
               ph[(q & 31) >> 1] = pack_f16x2(w0, w1);
             }
           }
-          tmem_st16(lane_base + col_p(j) + 16 * hf, ph);
+          // over the S buffer's first half: its scores are in registers
+          tmem_st16(lane_base + col_s(j, xb) + 16 * hf, ph);
         }
         l += sum * (1.0f / kPScale) * inv_f;
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(smem_u32(&ctl->p_full[j]));
+        mbar_arrive(smem_u32(&ctl->p_full[j][xb]));
       }
       g = g_first + seg_len;
       it.next_unit(ctl->pref, a.B, a.Hkv);
@@ -785,7 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (ok && had_page && warp_active) {
         long long g_last = g - 1;
         if ((int)(g_last & 1) != wg) --g_last;
-        ok = mbar_wait(smem_u32(&ctl->pv_done[wg]), (uint32_t)((g_last >> 1) & 1), abort_flag);
+        const long long n_last = g_last >> 1;
+        ok = mbar_wait(smem_u32(&ctl->pv_done[wg][n_last & 1]), (uint32_t)((n_last >> 1) & 1), abort_flag);
         fence_after_sync();
       }
       if (!ok) fail(ctl, a.status);
