@@ -141,6 +141,7 @@ size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, in
  * have been appended (causal inside the window).
  *   q   : bf16 [num_lanes][window][num_q_heads][128]   (|q| < 65504)
  *   out : bf16 [num_lanes][window][num_q_heads][128]   (written in full)
+ *   q and out must be 16-byte aligned (else SDVA_ERR_INVALID).
  *   window: 1 .. 16.   max_context: host upper bound on every L_b.
  *   workspace: device scratch of at least verify_attn_workspace_size(...) bytes,
  *     256-byte aligned, used only during the call's kernels (its contents

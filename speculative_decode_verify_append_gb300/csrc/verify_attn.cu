@@ -466,6 +466,8 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
                            int32_t* status, sdva_stream_t stream) {
   if (cache == nullptr || q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr)
     return SDVA_ERR_INVALID;
+  // q and out are read and written in 16-byte vectors (and q by bulk copies)
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return SDVA_ERR_INVALID;
   if (cache->k_codes == nullptr || cache->v_codes == nullptr || cache->k_scales == nullptr ||
       cache->v_scales == nullptr)
     return SDVA_ERR_INVALID;
@@ -484,7 +486,7 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SDVA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  if (tc::tc_supported(cache, num_lanes, window, num_q_heads, num_sms)) {
+  if (tc::tc_supported(cache, num_lanes, window, num_q_heads, max_pages_per_lane, num_sms)) {
     // <= 128 rows per kv head: tcgen05 kernels (FP8 or INT4 cache)
     if (workspace_bytes < tc::tc_workspace_bytes(num_lanes, window, num_q_heads, cache->num_kv_heads, num_sms))
       return SDVA_ERR_WORKSPACE;

@@ -119,6 +119,8 @@ struct Ctl {
   int abort;
   int stop;                   // set by warpgroup 0 at a segment end when the CTA gives up
   int pref[kMaxLanesTc + 1];  // pages per kv head of lanes < b (prefix)
+  int cp[kMaxLanesTc + 1];    // cost per kv head of lanes < b (see Partition)
+  long long range[2];         // this CTA's pages [start, end) of the flattened list
   int lens[kMaxLanesTc];      // L_b
 };
 
@@ -129,7 +131,101 @@ constexpr size_t smem_bytes() {
 static_assert(smem_bytes<SDVA_KV_FP8_E4M3>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<SDVA_KV_INT4_G32>() <= 232448, "shared memory budget");
 
-__device__ __forceinline__ long long cta_start(long long c, long long C, long long total) { return c * total / C; }
+// Partition of the flattened (lane, kv head, page) list over the CTAs.  Each
+// unit (lane, kv head) costs its pages plus kUnitCost: a CTA that starts a
+// new unit inside its range pays a segment end and a segment start (an
+// output epilogue, a Q row load and a pipeline refill, about the time of a
+// dozen pages), so equal shares of cost, not of pages, end together.  CTA c
+// owns the cost interval [c T / Ce, (c + 1) T / Ce), T the total cost and Ce
+// = min(CTAs, T), mapped to real pages: the cost of a unit's start maps to
+// its first page.
+constexpr int kUnitCost = 12;
+struct Partition {
+  const int* pref;  // [B + 1] pages per kv head of lanes < b
+  const int* cp;    // [B + 1] cost per kv head of lanes < b (pages + kUnitCost per lane with pages)
+  int B, Hkv;
+  __device__ long long total_pages() const { return (long long)Hkv * pref[B]; }
+  __device__ long long total_cost() const { return (long long)Hkv * cp[B]; }
+  __device__ long long ctas(int C) const { return min((long long)C, total_cost()); }
+  // real flattened page position of cost position y (0 <= y <= total cost).
+  // The offset inside a lane, below Hkv * (pages + kUnitCost), fits in 32
+  // bits: this path requires num_pages * Hkv * 64 < 2^31.
+  __device__ long long real_of(long long y) const {
+    if (y >= total_cost()) return total_pages();
+    int lo = 0, hi = B - 1;  // the lane of y: the last b with cost prefix <= y (it has pages)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)Hkv * cp[mid] <= y)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int nb = pref[lo + 1] - pref[lo];
+    const uint32_t r = (uint32_t)(y - (long long)Hkv * cp[lo]);
+    const uint32_t span = (uint32_t)(nb + kUnitCost);
+    const uint32_t q = r / span, v = r - q * span;
+    return (long long)Hkv * pref[lo] + (long long)q * nb + max(0, (int)v - kUnitCost);
+  }
+  // floor(c T / Ce), 0 <= c <= Ce <= 1024, in 32-bit arithmetic (T < 2^31):
+  // c T / Ce = c (T / Ce) + c (T % Ce) / Ce
+  __device__ long long cost_begin(long long c, long long Ce) const {
+    const uint32_t T = (uint32_t)total_cost(), ce = (uint32_t)Ce, cc = (uint32_t)c;
+    const uint32_t qT = T / ce, rT = T - qT * ce;
+    return (long long)(cc * qT + (cc * rT) / ce);
+  }
+  // first real position of CTA c of Ce (c = Ce: the end)
+  __device__ long long cta_begin(long long c, long long Ce) const { return real_of(cost_begin(c, Ce)); }
+  // the CTA of Ce whose cost interval holds cost position y (0 <= y < total
+  // cost).  The page at cost position y belongs to that CTA's page range:
+  // real_of is monotone and maps y back to the page.  An fp32 estimate, then
+  // exact steps.
+  __device__ long long cta_of_cost(long long y, long long Ce) const {
+    long long c = (long long)((float)y * (float)Ce / (float)total_cost());
+    c = max(0LL, min(c, Ce - 1));
+    while (c > 0 && cost_begin(c, Ce) > y) --c;
+    while (c + 1 < Ce && cost_begin(c + 1, Ce) <= y) ++c;
+    return c;
+  }
+};
+
+// Warp-wide prefix over lanes (one warp, all lanes): pref[b] = pages per kv
+// head of lanes < b and cp[b] = their cost (pages + kUnitCost per lane with
+// pages), b = 0 .. B; lens[b] = L_b when lens is not null.
+__device__ __forceinline__ void partition_prefix(const int32_t* seq_lens, int B, int W, int max_context, int max_pages,
+                                                 int lane, int* pref, int* cp, int* lens) {
+  int carry = 0, carry_c = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    int n = 0;
+    if (b < B) {
+      const int L = seq_lens[b];
+      if (lens) lens[b] = L;
+      const bool ok = L >= 0 && L <= max_context && (long long)L + W <= (long long)max_pages * kPage;
+      n = ok ? (L + W + kPage - 1) / kPage : 0;
+    }
+    const int cost = n > 0 ? n + kUnitCost : 0;
+    int incl = n, incl_c = cost;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      const int yc = __shfl_up_sync(0xffffffffu, incl_c, o);
+      if (lane >= o) {
+        incl += y;
+        incl_c += yc;
+      }
+    }
+    if (b < B) {
+      pref[b] = carry + incl - n;
+      cp[b] = carry_c + incl_c - cost;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+    carry_c += __shfl_sync(0xffffffffu, incl_c, 31);
+  }
+  if (lane == 0) {
+    pref[B] = carry;
+    cp[B] = carry_c;
+  }
+}
 
 // Walks the flattened (lane, kv head, page) list in order.
 struct PageIter {
@@ -289,28 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const int C = gridDim.x, c = blockIdx.x;
   volatile int* abort_flag = &ctl->abort;
 
-  // ---- partition: pages per kv head of every lane, prefix over lanes ----
+  // ---- partition: pages and cost per kv head of every lane, prefix over lanes ----
   if (warp == 0) {
-    int carry = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int n = 0;
-      if (b < a.B) {
-        const int L = a.seq_lens[b];
-        ctl->lens[b] = L;
-        const bool ok = L >= 0 && L <= a.max_context && (long long)L + a.W <= (long long)a.max_pages * kPage;
-        n = ok ? (L + a.W + kPage - 1) / kPage : 0;
-      }
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (b < a.B) ctl->pref[b] = carry + incl - n;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, lane, ctl->pref, ctl->cp, ctl->lens);
+    __syncwarp();
+    if (lane == 0) {
+      // this CTA's page range [start, end)
+      const Partition part{ctl->pref, ctl->cp, a.B, a.Hkv};
+      const long long Ce = part.ctas(C);
+      ctl->range[0] = c < Ce ? part.cta_begin(c, Ce) : 0;
+      ctl->range[1] = c < Ce ? part.cta_begin(c + 1, Ce) : 0;
     }
-    if (lane == 0) ctl->pref[a.B] = carry;
   }
   // only the softmax warps that own query rows take part in the page protocol
   const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);
@@ -340,12 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     mbar_fence_init();
   }
   __syncthreads();
-  const long long total = (long long)a.Hkv * ctl->pref[a.B];
-  // pages are spread over min(C, total) CTAs, so every CTA of that set owns at least one
-  const long long Ce = min((long long)C, total);
-  const long long start = c < Ce ? cta_start(c, Ce, total) : 0, end = c < Ce ? cta_start(c + 1, Ce, total) : 0;
+  const long long start = ctl->range[0], end = ctl->range[1];
   const long long n_local = end - start;
-  if (n_local <= 0) return;  // uniform for the whole CTA
+  // uniform for the whole CTA (a range inside a unit's start cost has no pages)
+  if (n_local <= 0) return;
 
   if (warp == kProducerWarp) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
   fence_before_sync();
@@ -907,39 +990,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
 }
 
 // Merge prologue, run by warp 0 of a block: whether lane b's length fits, and
-// the first and last CTA whose page range holds part of unit (b, hk) (same
-// partition rule as the split kernel).
-__device__ __forceinline__ bool merge_locate(const TcArgs& a, int C, int b, int hk, int warp, int lane,
-                                             long long* s_first, long long* s_last) {
+// the first and last CTA whose page range holds part of unit (b, hk) (the
+// split kernel's partition, from the same prefix arrays).  pref and cp are
+// shared-memory arrays of B + 1 entries.
+__device__ __forceinline__ bool merge_locate(const TcArgs& a, int C, int b, int hk, int warp, int lane, int* pref,
+                                             int* cp, long long* s_first, long long* s_last) {
   const int L = a.seq_lens[b];
   const bool len_ok = L >= 0 && L <= a.max_context && (long long)L + a.W <= (long long)a.max_pages * kPage;
-  const int nb = len_ok ? (L + a.W + kPage - 1) / kPage : 0;
   if (warp == 0) {
-    long long before = 0, all = 0;
-    for (int bb = lane; bb < a.B; bb += 32) {
-      const int Lb = a.seq_lens[bb];
-      const bool ok = Lb >= 0 && Lb <= a.max_context && (long long)Lb + a.W <= (long long)a.max_pages * kPage;
-      const int n = ok ? (Lb + a.W + kPage - 1) / kPage : 0;
-      all += n;
-      if (bb < b) before += n;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-      all += __shfl_xor_sync(0xffffffffu, all, o);
-    }
+    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, lane, pref, cp, nullptr);
+    __syncwarp();
     if (lane == 0 && len_ok) {
-      const long long total = (long long)a.Hkv * all;
-      const long long Pu = (long long)a.Hkv * before + (long long)hk * nb;
-      const long long Ce = min((long long)C, total);  // CTAs that own pages (each at least one)
-      auto locate = [&](long long x) {
-        long long cc = x * Ce / total;
-        while (cc + 1 < Ce && cta_start(cc + 1, Ce, total) <= x) ++cc;
-        while (cc > 0 && cta_start(cc, Ce, total) > x) --cc;
-        return cc;
-      };
-      *s_first = locate(Pu);
-      *s_last = locate(Pu + nb - 1);
+      const Partition part{pref, cp, a.B, a.Hkv};
+      const int nb = pref[b + 1] - pref[b];
+      // cost position of the unit's first page (after its start cost)
+      const long long y0 = (long long)a.Hkv * cp[b] + (long long)hk * (nb + kUnitCost) + kUnitCost;
+      const long long Ce = part.ctas(C);
+      *s_first = part.cta_of_cost(y0, Ce);
+      *s_last = part.cta_of_cost(y0 + nb - 1, Ce);
     }
   }
   return len_ok;
@@ -952,7 +1020,8 @@ __global__ void __launch_bounds__(256) verify_merge_rows_tc_kernel(TcArgs a, int
   const int b = u / a.Hkv, hk = u % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ long long s_first, s_last;
-  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, &s_first, &s_last);
+  __shared__ int s_pref[kMaxLanesTc + 1], s_cp[kMaxLanesTc + 1];
+  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, s_pref, s_cp, &s_first, &s_last);
   __syncthreads();
   // programmatic dependent of the split kernel (see verify_merge_tc_kernel)
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1041,7 +1110,8 @@ __global__ void __launch_bounds__(kMergeThreads) verify_merge_tc_kernel(TcArgs a
   __shared__ float s_M, s_inv;
   __shared__ int s_bad;
   __shared__ float4 s_acc[kMergeThreads / 32][32];
-  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, &s_first, &s_last);
+  __shared__ int s_pref[kMaxLanesTc + 1], s_cp[kMaxLanesTc + 1];
+  const bool len_ok = merge_locate(a, C, b, hk, warp, lane, s_pref, s_cp, &s_first, &s_last);
   __syncthreads();
   // launched as a programmatic dependent of the split kernel: everything
   // above overlapped its tail; its partials and rows are visible after this
@@ -1163,11 +1233,13 @@ size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms) {
   return ml + slots * R * kHeadDim * sizeof(float);
 }
 
-bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms) {
+bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_pages, int num_sms) {
   const int Hkv = cache->num_kv_heads;
   const int R = W * (Hq / Hkv);
   const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || (cache->dtype == SDVA_KV_FP8_E4M3 && encoder() != nullptr);
-  return dtype_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 && num_sms <= kMaxSegments &&
+  // the partition's cost arithmetic is 32-bit (see Partition)
+  const bool cost_ok = (long long)B * (max_pages + kUnitCost) * Hkv < (1LL << 31);
+  return dtype_ok && cost_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 && num_sms <= kMaxSegments &&
          (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }
 

@@ -32,7 +32,7 @@ struct TcArgs {
 // Scratch bytes of the tcgen05 path (split-K partials, one slot per unit and per CTA).
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms);
 // Whether the tcgen05 path handles this call (<= 128 rows per kv head, ...).
-bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int num_sms);
+bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_pages, int num_sms);
 // Enqueue the split and merge kernels on `stream`.
 int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream);
 

@@ -110,6 +110,10 @@ def test_argument_validation_returns_before_cuda(lib):
     c.num_kv_heads = 1
     assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, -1.0, fake, fake, 1 << 20, None, None) == -1
     assert va(ctypes.byref(c), None, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
+    # q and out are read and written in 16-byte vectors: both must be 16-byte aligned
+    odd = P(0x1008)
+    assert va(ctypes.byref(c), odd, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
+    assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, 0.088, odd, fake, 1 << 20, None, None) == -1
     sa = lib.spec_accept
     sa.restype = ctypes.c_int
     assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
