@@ -16,8 +16,10 @@ One JSON line (rank 0):
   clocks       nvidia-smi SM clocks and throttle reasons during the timed steps
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an untimed L2
-flush (a 512 MB write), each bracketed by CUDA events on the launching stream;
-a barrier and a device synchronize bracket the whole timed loop.
+flush (a 512 MB write, then a 512 MB read of a second buffer, so that L2 holds
+none of the step's inputs and none of the write's dirty lines), each bracketed
+by CUDA events on the launching stream; a barrier and a device synchronize
+bracket the whole timed loop.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 Multi-GPU: torchrun, one replica per GPU (lanes are independent: no collective).
@@ -46,8 +48,9 @@ METRIC = "verify_attn HBM GB/s (% of GB300 peak) and verify steps/s at 8 lanes"
 DEFAULT_WORKLOAD = "multi_lane"
 # dram bytes (read + write) of one verify_attn call (split + merge kernels),
 # measured by ncu for the current kernels, per workload (absent: not captured
-# for this workload, reported as null).  Source: profiles/verify_split_tc_fp8_multi_lane.md
-NCU_TRAFFIC_BYTES: dict = {}
+# for this workload, reported as null).  Source: the ncu launch-list summary
+# of the multi-lane workload under profiles/.
+NCU_TRAFFIC_BYTES = {"multi_lane": 305_102_336 + 562_432 + 8_768_256}
 
 
 def workload_desc(spec: synth.Spec) -> str:
@@ -290,6 +293,14 @@ def run_gpu(args):
     drafts = torch.from_numpy(step.drafts).to(dev) if step.drafts is not None else None
     vs = VerifyStep(B, W, Hq, Hkv, max_context, spec.vocab, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # The write evicts the step's inputs; the read of a second buffer then
+        # evicts the write's dirty lines, whose write-back would otherwise land
+        # inside the timed step.
+        flush.zero_()
+        clean.amax()
     stream = torch.cuda.current_stream()
 
     def one_step(evs=None):
@@ -307,7 +318,7 @@ def run_gpu(args):
             evs[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         one_step()
     torch.cuda.synchronize()
     assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
@@ -326,7 +337,7 @@ def run_gpu(args):
     wall0 = time.perf_counter()
     torch.cuda.nvtx.range_push("timed_steps")
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         one_step(evs[k])
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
@@ -356,7 +367,7 @@ def run_gpu(args):
     e2e_steps = max(10, min(args.steps, 200))
     e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
     for k in range(e2e_steps + 3):
-        flush.zero_()
+        flush_l2()
         if k >= 3:
             e_ev[k - 3][0].record(stream)
         for n, t in host_in.items():
@@ -388,7 +399,7 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, N(0,1) fp32 logits)",
         "config": {"workload": workload_desc(spec), "lanes": B, "window": W, "q_heads": Hq, "kv_heads": Hkv,
                    "context_tokens": int(step.seq_lens.sum()), "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (512 MB write, untimed)"},
+                   "l2": "flushed before every timed step (512 MB write, then 512 MB read of a second buffer; untimed)"},
         "verify_attn": {"us": att_ms * 1e3, "gbs": achieved, "pct_of_peak": 100.0 * achieved / peak,
                         "algorithmic_bytes": alg},
         "breakdown_us": {"kv_append_quant": float(np.mean(t_app)) * 1e3, "verify_attn": att_ms * 1e3,

@@ -134,12 +134,12 @@ static_assert(smem_bytes<SDVA_KV_INT4_G32>() <= 232448, "shared memory budget");
 // Partition of the flattened (lane, kv head, page) list over the CTAs.  Each
 // unit (lane, kv head) costs its pages plus kUnitCost: a CTA that starts a
 // new unit inside its range pays a segment end and a segment start (an
-// output epilogue, a Q row load and a pipeline refill, about the time of a
-// dozen pages), so equal shares of cost, not of pages, end together.  CTA c
+// output epilogue, a Q row load and a pipeline refill, measured at about the
+// time of 12-16 pages), so equal shares of cost, not of pages, end together.  CTA c
 // owns the cost interval [c T / Ce, (c + 1) T / Ce), T the total cost and Ce
 // = min(CTAs, T), mapped to real pages: the cost of a unit's start maps to
 // its first page.
-constexpr int kUnitCost = 12;
+constexpr int kUnitCost = 16;
 struct Partition {
   const int* pref;  // [B + 1] pages per kv head of lanes < b
   const int* cp;    // [B + 1] cost per kv head of lanes < b (pages + kUnitCost per lane with pages)
