@@ -389,12 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   if (warp == 0) {
     partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, lane, ctl->pref, ctl->cp, ctl->lens);
     __syncwarp();
-    if (lane == 0) {
-      // this CTA's page range [start, end)
+    if (lane < 2) {
+      // this CTA's page range [start, end): start on lane 0, end on lane 1
       const Partition part{ctl->pref, ctl->cp, a.B, a.Hkv};
       const long long Ce = part.ctas(C);
-      ctl->range[0] = c < Ce ? part.cta_begin(c, Ce) : 0;
-      ctl->range[1] = c < Ce ? part.cta_begin(c + 1, Ce) : 0;
+      ctl->range[lane] = c < Ce ? part.cta_begin(c + lane, Ce) : 0;
     }
   }
   // only the softmax warps that own query rows take part in the page protocol
