@@ -8,7 +8,9 @@
 //
 // Kernel 1 (argmax): one thread-block cluster of up to 8 CTAs per logits
 // row; each CTA scans a contiguous slice of the row with 16-byte streaming
-// loads, eight in flight per thread, reduces (value, index) in shared memory,
+// loads, four in flight per thread (32 registers, so eight 256-thread CTAs fit
+// on an SM and the grid of the multi-row case is a single wave), reduces
+// (value, index) in shared memory,
 // and stores it into CTA rank 0's shared memory through distributed shared
 // memory; rank 0 writes the row's argmax.  No global scratch.  Ties go to the
 // lowest index, NaN never wins, an all-NaN row gives 0.
@@ -50,7 +52,7 @@ __device__ __forceinline__ void take4(const float4 v, int i, float& bv, int& bi)
 }
 
 // grid (parts, rows), cluster (parts, 1, 1)
-__global__ void __launch_bounds__(kArgmaxThreads) argmax_rows_kernel(const float* logits, int vocab, int chunk,
+__global__ void __launch_bounds__(kArgmaxThreads, 8) argmax_rows_kernel(const float* logits, int vocab, int chunk,
                                                                     int32_t* out_tokens) {
   cg::cluster_group cluster = cg::this_cluster();
   // the finalize kernel may be scheduled now; it waits for this grid's results
@@ -66,12 +68,12 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_rows_kernel(const float
     const int step = blockDim.x;
     int k = lo / 4 + threadIdx.x;
     const int kend = hi / 4;
-    for (; k + 7 * step < kend; k += 8 * step) {
-      float4 v[8];
+    for (; k + 3 * step < kend; k += 4 * step) {
+      float4 v[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcs(x4 + k + u * step);
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + k + u * step);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) take4(v[u], 4 * (k + u * step), bv, bi);
+      for (int u = 0; u < 4; ++u) take4(v[u], 4 * (k + u * step), bv, bi);
     }
     for (; k < kend; k += step) take4(__ldcs(x4 + k), 4 * k, bv, bi);
   } else {
