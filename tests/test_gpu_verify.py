@@ -45,6 +45,10 @@ SMALL = [
     (synth.KV_INT4, [0, 64, 129, 900], 8, 24, 4),
     (synth.KV_INT4, [1200, 77], 16, 12, 2),
     (synth.KV_INT4, [700], 1, 4, 1),
+    # many short lanes: CTAs cross several unit boundaries and most units span
+    # several CTAs; some CTAs' cost shares fall inside a unit's start cost
+    (synth.KV_FP8, [(37 * i) % 300 for i in range(40)], 16, 24, 4),
+    (synth.KV_INT4, [(53 * i) % 400 for i in range(24)], 8, 24, 4),
 ]
 
 
