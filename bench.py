@@ -51,7 +51,7 @@ DEFAULT_WORKLOAD = "multi_lane"
 # measured by ncu for the current kernels, per workload (absent: not captured
 # for this workload, reported as null).  Source: the ncu launch-list summary
 # of the multi-lane workload under profiles/.
-NCU_TRAFFIC_BYTES = {"multi_lane": 305_078_016 + 746_752 + 8_818_432 + 2_304}
+NCU_TRAFFIC_BYTES = {"multi_lane": 305_100_032 + 742_400 + 8_818_432}
 
 
 def workload_desc(spec: synth.Spec) -> str:
