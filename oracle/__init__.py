@@ -72,6 +72,8 @@ def _load():
             lib.oracle_argmax.argtypes = [P, I]
             lib.oracle_spec_accept.restype = I
             lib.oracle_spec_accept.argtypes = [P, I, I, I, P, P, P, P, P]
+            lib.oracle_spec_accept_lazy.restype = I
+            lib.oracle_spec_accept_lazy.argtypes = [P, I, I, I, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -218,4 +220,21 @@ def spec_accept(logits: np.ndarray, drafts: np.ndarray, seq_lens: np.ndarray | N
     st = np.zeros(1, np.int32)
     _load().oracle_spec_accept(_ptr(lg), B, W, V, _ptr(dr) if dr.size else None, _ptr(acc), _ptr(tok), _ptr(sl),
                                _ptr(st))
+    return acc, tok, sl, int(st[0])
+
+
+def spec_accept_lazy(logits: np.ndarray, drafts: np.ndarray, num_drafts: np.ndarray | None = None,
+                     seq_lens: np.ndarray | None = None):
+    """Lazy acceptance with per-lane draft counts (None: window - 1 each).
+    Returns (accept_len [B], out_tokens [B][W] with -1 after row a, new seq_lens or None, status)."""
+    lg = _as(logits, np.float32)
+    B, W, V = lg.shape
+    dr = _as(drafts, np.int32).reshape(B, W - 1) if W > 1 else np.zeros((B, 0), np.int32)
+    nd = None if num_drafts is None else _as(num_drafts, np.int32).reshape(B)
+    acc = np.zeros(B, np.int32)
+    tok = np.zeros((B, W), np.int32)
+    sl = None if seq_lens is None else _as(seq_lens, np.int32).copy()
+    st = np.zeros(1, np.int32)
+    _load().oracle_spec_accept_lazy(_ptr(lg), B, W, V, _ptr(dr) if dr.size else None, _ptr(nd), _ptr(acc),
+                                    _ptr(tok), _ptr(sl), _ptr(st))
     return acc, tok, sl, int(st[0])

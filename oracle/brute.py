@@ -180,3 +180,12 @@ def accept(logits_rows, drafts):
     while a < len(drafts) and drafts[a] == t[a]:
         a += 1
     return a, t
+
+
+def accept_lazy(logits_rows, drafts, d):
+    """Per-lane draft count d (0 <= d <= len(drafts)).  a is the largest k <= d
+    such that the first k drafts equal the first k argmaxes; the argmaxes of
+    rows 0 .. a are reported and -1 after them.  Returns (a, tokens)."""
+    t = [argmax(r) for r in logits_rows]
+    a = max(k for k in range(d + 1) if all(drafts[i] == t[i] for i in range(k)))
+    return a, t[:a + 1] + [-1] * (len(logits_rows) - a - 1)

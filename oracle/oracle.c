@@ -42,6 +42,11 @@
  *      gives 0; -0 and +0 compare equal.  drafts[i] is checked against the
  *      argmax of window position i; accept length a = leading matches; the
  *      commit adds 1 + a to the lane's length.
+ *   R7 A lane may carry fewer drafts than the window holds (the draft count is
+ *      chosen per workload, NInfer review section "아키텍처 ③"): with d_b
+ *      drafts only drafts[b][0 .. d_b) are compared, and the rows after the
+ *      first disagreement decide nothing, so the lazy form reports argmaxes
+ *      only for rows 0 .. a and -1 after them.
  *
  * Arithmetic: codecs in IEEE fp32 exactly as stated (compiled with
  * -ffp-contract=off, no fast-math); attention in fp64, two-pass softmax.
@@ -55,7 +60,7 @@
 #define PAGE 64
 #define HEAD_DIM 128
 
-enum { ST_BAD_PAGE = 1, ST_OVERFLOW = 2, ST_BAD_DRAFT = 4 };
+enum { ST_BAD_PAGE = 1, ST_OVERFLOW = 2, ST_BAD_DRAFT = 4, ST_BAD_COUNT = 16 };
 enum { KV_FP8 = 0, KV_INT4 = 1 };
 
 /* ------------------------------------------------------------------ */
@@ -576,6 +581,46 @@ int oracle_spec_accept(const float* logits, int num_lanes, int window, int vocab
                 *status |= ST_BAD_DRAFT;
         while (a < d && drafts[b * d + a] == out_tokens[b * window + a])
             ++a;
+        accept_len[b] = a;
+        if (seq_lens_inout)
+            seq_lens_inout[b] += 1 + a;
+    }
+    return 0;
+}
+
+/* Lazy acceptance with per-lane draft counts (R6, R7).
+ * num_drafts [B] may be NULL (every lane has window - 1 drafts).  A lane whose
+ * count is outside [0, window - 1] sets ST_BAD_COUNT and gets accept_len 0,
+ * out_tokens all -1 and no commit.  Otherwise: every one of the lane's d_b
+ * drafts outside [0, vocab) sets ST_BAD_DRAFT (and never matches); rows are
+ * taken in order, row i's argmax is reported, and the walk stops at the first
+ * i that is d_b or whose draft disagrees; a = that i is the accept length,
+ * out_tokens after row a are -1, and the commit adds 1 + a. */
+int oracle_spec_accept_lazy(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
+                            const int32_t* num_drafts, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* seq_lens_inout, int32_t* status)
+{
+    int b, i, dmax = window - 1;
+    for (b = 0; b < num_lanes; ++b) {
+        int d = num_drafts ? num_drafts[b] : dmax, a = 0;
+        for (i = 0; i < window; ++i)
+            out_tokens[b * window + i] = -1;
+        if (d < 0 || d > dmax) {
+            accept_len[b] = 0;
+            if (status)
+                *status |= ST_BAD_COUNT;
+            continue;
+        }
+        for (i = 0; i < d; ++i)
+            if ((drafts[b * dmax + i] < 0 || drafts[b * dmax + i] >= vocab) && status)
+                *status |= ST_BAD_DRAFT;
+        for (;;) {
+            int t = oracle_argmax(logits + ((size_t)b * window + a) * vocab, vocab);
+            out_tokens[b * window + a] = t;
+            if (a == d || drafts[b * dmax + a] != t)
+                break;
+            ++a;
+        }
         accept_len[b] = a;
         if (seq_lens_inout)
             seq_lens_inout[b] += 1 + a;

@@ -71,3 +71,86 @@ def test_mean_accept_length_closed_form(d, p):
     # standard error of the mean is below 0.05 at these sizes; allow 4 sigma
     var = np.var(acc)
     assert abs(acc.mean() - want) < 4 * np.sqrt(var / lanes) + 1e-9
+
+
+# ---- lazy acceptance with per-lane draft counts --------------------------
+
+def test_lazy_matches_brute_with_per_lane_counts():
+    rng = np.random.default_rng(14)
+    for trial in range(40):
+        B, W, V = 4, 1 + trial % 7, 30
+        logits = rng.integers(-3, 4, size=(B, W, V)).astype(np.float32)  # many ties
+        logits[0, rng.integers(0, W), rng.integers(0, V, size=5)] = np.nan
+        targets = logits.argmax(axis=2)
+        drafts = np.where(rng.random((B, W - 1)) < 0.6, targets[:, :W - 1],
+                          rng.integers(0, V, size=(B, W - 1))).astype(np.int32)
+        nd = rng.integers(0, W, size=B).astype(np.int32)
+        L = np.array([3, 1, 4, 1], np.int32)
+        acc, tok, sl, st = oracle.spec_accept_lazy(logits, drafts, nd, L)
+        assert st == 0
+        for b in range(B):
+            a, t = brute.accept_lazy(logits[b].tolist(), [int(x) for x in drafts[b]], int(nd[b]))
+            assert acc[b] == a and list(tok[b]) == t, (trial, b)
+            assert sl[b] == L[b] + 1 + a
+
+
+def test_lazy_rows_after_the_first_disagreement_decide_nothing():
+    rng = np.random.default_rng(15)
+    B, W, V = 6, 9, 200
+    logits = rng.standard_normal((B, W, V)).astype(np.float32)
+    targets = logits.argmax(axis=2)
+    drafts = np.where(rng.random((B, W - 1)) < 0.7, targets[:, :W - 1], (targets[:, :W - 1] + 1) % V)
+    drafts = drafts.astype(np.int32)
+    acc, tok, _, _ = oracle.spec_accept_lazy(logits, drafts)
+    poisoned = logits.copy()
+    for b in range(B):
+        poisoned[b, acc[b] + 1:, :] = np.nan
+        poisoned[b, acc[b] + 1:, 7] = np.inf
+    acc2, tok2, _, _ = oracle.spec_accept_lazy(poisoned, drafts)
+    assert np.array_equal(acc, acc2) and np.array_equal(tok, tok2)
+    # the eager rule agrees on the accept length and on rows 0 .. a
+    acc3, tok3, _, _ = oracle.spec_accept(logits, drafts)
+    assert np.array_equal(acc, acc3)
+    for b in range(B):
+        assert list(tok[b, :acc[b] + 1]) == list(tok3[b, :acc[b] + 1])
+        assert (tok[b, acc[b] + 1:] == -1).all()
+
+
+def test_lazy_counts_zero_full_and_invalid():
+    spec = synth.WORKLOADS["tiny"]
+    logits, drafts, targets = synth.acceptance_inputs(spec, 5, 6, 300, 1.0)
+    # every draft agrees: a = d_b, bonus = the target at row d_b
+    nd = np.array([0, 1, 5, 3, 2], np.int32)
+    acc, tok, sl, st = oracle.spec_accept_lazy(logits, drafts, nd, np.zeros(5, np.int32))
+    assert list(acc) == list(nd) and st == 0 and list(sl) == list(1 + nd)
+    for b in range(5):
+        assert list(tok[b, :nd[b] + 1]) == list(targets[b, :nd[b] + 1]) and (tok[b, nd[b] + 1:] == -1).all()
+    # no count array means window - 1 drafts everywhere
+    acc, tok, _, _ = oracle.spec_accept_lazy(logits, drafts)
+    assert (acc == 5).all() and np.array_equal(tok, targets)
+    # a count outside [0, window - 1]: flagged, lane skipped, no commit
+    nd = np.array([-1, 6, 2, 0, 5], np.int32)
+    acc, tok, sl, st = oracle.spec_accept_lazy(logits, drafts, nd, np.full(5, 10, np.int32))
+    assert st == 16 and list(acc) == [0, 0, 2, 0, 5]
+    assert (tok[:2] == -1).all() and list(sl) == [10, 10, 13, 11, 16]
+
+
+def test_lazy_bad_drafts_only_within_the_lane_count():
+    logits = np.zeros((2, 4, 8), np.float32)
+    logits[:, :, 2] = 1.0
+    drafts = np.array([[2, 2, 99], [2, -5, 2]], np.int32)
+    _, _, _, st = oracle.spec_accept_lazy(logits, drafts, np.array([2, 1], np.int32))
+    assert st == 0  # the bad ids lie past each lane's count
+    acc, _, _, st = oracle.spec_accept_lazy(logits, drafts, np.array([3, 2], np.int32))
+    assert st == 4 and list(acc) == [2, 1]
+
+
+@pytest.mark.parametrize("p", [0.7, 0.5])
+def test_lazy_mean_accept_length_closed_form_per_lane_count(p):
+    spec = synth.WORKLOADS["tiny"]
+    lanes, W = 4000, 10
+    logits, drafts, _ = synth.acceptance_inputs(spec, lanes, W, 64, p, tag=f"lazy{p}")
+    nd = (np.arange(lanes) % W).astype(np.int32)
+    acc, _, _, _ = oracle.spec_accept_lazy(logits, drafts, nd)
+    want = np.mean([sum(p ** k for k in range(1, int(d) + 1)) for d in nd])
+    assert abs(acc.mean() - want) < 4 * np.sqrt(np.var(acc) / lanes) + 1e-9
