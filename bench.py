@@ -14,6 +14,9 @@ One JSON line (rank 0):
                host->device inputs and device->host results inside the timing
                (the logits copy overlaps append and verify: only accept reads it)
   cpu_baseline the CPU oracle on the host cores, on a bounded sample
+  spec_accept_lazy  the acceptance that reads each lane's logits rows only up
+               to its first disagreement (timed apart, after the main loop),
+               with the step rate it would give
   clocks       nvidia-smi SM clocks and throttle reasons during the timed steps
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an untimed L2
@@ -353,6 +356,39 @@ def run_gpu(args):
     ms_per_step = total_ms / args.steps
     value = world * args.steps / (total_ms / 1e3)
 
+    # ---- lazy acceptance (rows read only up to each lane's first disagreement) ----
+    lazy = None
+    if logits is not None:
+        l_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for k in range(args.warmup + args.steps):
+            flush_l2()
+            if k >= args.warmup:
+                l_ev[k - args.warmup][0].record(stream)
+            vs.accept_lazy(logits, drafts, None, commit_lens)
+            if k >= args.warmup:
+                l_ev[k - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        acc_lazy = vs.accept_len.cpu().numpy().copy()
+        tok_lazy = vs.out_tokens.cpu().numpy().copy()
+        vs.accept(logits, drafts, None)
+        torch.cuda.synchronize()
+        acc_eager, tok_eager = vs.accept_len.cpu().numpy(), vs.out_tokens.cpu().numpy()
+        assert np.array_equal(acc_lazy, acc_eager), (acc_lazy, acc_eager)
+        for b in range(B):
+            assert np.array_equal(tok_lazy[b, :acc_lazy[b] + 1], tok_eager[b, :acc_lazy[b] + 1])
+        assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
+        t_lazy = float(np.mean([e[0].elapsed_time(e[1]) for e in l_ev]))
+        walk = B >= sdva.LAZY_WALK_MIN_LANES
+        rows_needed = int((1 + acc_lazy).sum())
+        rows_read = rows_needed if walk else B * W
+        lazy_bytes = rows_read * spec.vocab * 4 + B * (W - 1) * 4
+        lazy_step_us = (float(np.mean(t_app)) + float(np.mean(t_att)) + t_lazy) * 1e3
+        lazy = {"us": t_lazy * 1e3, "mode": "walk" if walk else "parallel", "rows_needed": rows_needed,
+                "rows_read": rows_read, "rows_in_window": B * W, "accept_len": [int(a) for a in acc_lazy],
+                "bytes_read": lazy_bytes, "gbs": lazy_bytes / (t_lazy / 1e3) / 1e9,
+                "eager_us": float(np.mean(t_acc)) * 1e3, "step_us": lazy_step_us, "steps_per_s": 1e6 / lazy_step_us,
+                "timing": "CUDA events around the call after an L2 flush, same steps and warm-up as the main loop"}
+
     # ---- e2e: host buffers through the public API ----
     host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("kw", kw), ("vw", vw))}
     if logits is not None:
@@ -432,6 +468,7 @@ def run_gpu(args):
                      "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "algorithmic_bytes": alg},
         "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "spec_accept_lazy": lazy,
         "gpu_launches": args.steps * (1 + 2 + (2 if logits is not None else 0)),
         "clocks": clocks,
         "wall_s_timed_loop": wall,
@@ -462,6 +499,54 @@ def run_gpu(args):
     return 0
 
 
+def run_lazy_sweep(args):
+    """Eager vs lazy acceptance over lane counts: 151,936 fp32 logits per row,
+    16 positions, drafts agreeing with the argmax with probability 0.7 (seeded
+    device RNG), L2 flushed before every call; one JSON line of mean us."""
+    import torch
+
+    import speculative_decode_verify_append_gb300 as sdva
+    dev = torch.device("cuda", 0)
+    V, W, p = 151936, 16, 0.7
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    res = {}
+    for B in (8, 16, 32, 48, 64, 128):
+        logits = torch.randn((B, W, V), generator=gen, device=dev)
+        t = logits.argmax(dim=2).to(torch.int32)
+        agree = torch.rand((B, W - 1), generator=gen, device=dev) < p
+        drafts = torch.where(agree, t[:, :W - 1], (t[:, :W - 1] + 1) % V).to(torch.int32).contiguous()
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        tok = torch.zeros((B, W), dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        row = {}
+        for name, fn in (("eager_us", lambda: sdva.spec_accept(logits, drafts, acc, tok, None, st)),
+                         ("lazy_us", lambda: sdva.spec_accept_lazy(logits, drafts, acc, tok, None, None, st))):
+            evs = []
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                clean.amax()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                if k >= args.warmup:
+                    evs.append((e0, e1))
+            torch.cuda.synchronize()
+            row[name] = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        assert int(st.item()) == 0, sdva.sdva_status_string(int(st.item()))
+        row["mode"] = "walk" if B >= sdva.LAZY_WALK_MIN_LANES else "parallel"
+        row["max_accept_len"] = int(acc.max().item())
+        row["rows_needed"] = int((acc + 1).sum().item())
+        res[str(B)] = row
+        del logits
+    print(json.dumps({"lazy_sweep": res, "vocab": V, "window": W, "p": p, "steps": args.steps,
+                      "warmup": args.warmup}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,9 +555,13 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lazy-sweep", action="store_true",
+                    help="time spec_accept vs spec_accept_lazy over lane counts instead of the step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.lazy_sweep:
+        return run_lazy_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

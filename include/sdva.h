@@ -18,6 +18,8 @@
  *                       lane's window over its whole cached context
  *   spec_accept      -- argmax per window position, longest agreeing draft
  *                       prefix, optional commit of the new lengths
+ *   spec_accept_lazy -- the same acceptance reading each lane's rows only up
+ *                       to its first disagreement, with per-lane draft counts
  *
  * Conventions for every call
  *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA
@@ -104,6 +106,7 @@ typedef struct {
 #define SDVA_STATUS_OVERFLOW 2  /* L_b < 0, or L_b + n does not fit the lane's row / max_context */
 #define SDVA_STATUS_BAD_DRAFT 4 /* a draft id is outside [0, vocab) */
 #define SDVA_STATUS_TIMEOUT 8   /* a bounded device wait gave up */
+#define SDVA_STATUS_BAD_COUNT 16 /* a per-lane draft count is outside [0, window - 1] */
 
 /*
  * kv_append_quant -- write tokens [L_b, L_b + n_new) of every lane into the
@@ -208,6 +211,42 @@ int verify_attn_noalloc(const sdva_kv_cache* cache, const void* q, int num_q_hea
 int spec_accept(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
                 int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout, int32_t* status,
                 sdva_stream_t stream);
+
+/*
+ * spec_accept_lazy -- greedy acceptance that reads a lane's logits rows only
+ * up to its first disagreement, with a draft count per lane.
+ *   The accepted prefix ends at the first draft that disagrees with the
+ *   target argmax (Baseten talk summary, section "추측 디코드"), so the rows
+ *   after it decide nothing; the draft count is chosen per workload (NInfer
+ *   review, section "아키텍처 ③"), and a batch may mix lanes that drafted
+ *   different numbers of tokens into one padded window.
+ *   logits, drafts, seq_lens_inout: as for spec_accept (drafts keeps the
+ *               row stride window - 1; entries past a lane's count are not
+ *               read).
+ *   num_drafts: nullable int32 [num_lanes]: d_b, the lane's draft count,
+ *               0 <= d_b <= window - 1; NULL means window - 1 for every lane.
+ *               Rows past d_b are never read.
+ *   accept_len: int32 [num_lanes] (out): a = number of leading i < d_b with
+ *               drafts[b][i] == argmax of row i.
+ *   out_tokens: int32 [num_lanes][window] (out): the argmax of rows 0 .. a
+ *               (same tie rules as spec_accept; the bonus token is
+ *               out_tokens[b][a]) and -1 in every later position.
+ * With SDVA_LAZY_WALK_MIN_LANES (48) lanes or more a lane reads rows 0 .. a
+ * from memory (one CTA
+ * cluster walks them in order) and may prefetch row a + 1 into L2; with fewer
+ * lanes, where that serial walk is slower than one pass over the GPU, rows
+ * 0 .. d_b of every lane are reduced at once.  Both give the same results.
+ * A lane whose count is outside
+ * [0, window - 1] sets SDVA_STATUS_BAD_COUNT and gets accept_len 0,
+ * out_tokens all -1 and no commit.  An out-of-vocabulary id among a lane's
+ * first d_b drafts sets SDVA_STATUS_BAD_DRAFT and never matches.
+ * Limits and return codes as for spec_accept.
+ */
+#define SDVA_LAZY_WALK_MIN_LANES 48 /* spec_accept_lazy walks rows from this many lanes on */
+
+int spec_accept_lazy(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
+                     const int32_t* num_drafts, int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout,
+                     int32_t* status, sdva_stream_t stream);
 
 /* Static description of a return code or status bit set (never NULL). */
 const char* sdva_status_string(int code);

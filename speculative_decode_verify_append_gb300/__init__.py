@@ -11,6 +11,8 @@ The calls mirror ``include/sdva.h``:
     verify_attn_workspace_size(num_lanes, window, num_q_heads, num_kv_heads, max_context, num_sms=0)
     verify_attn(cache, q, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None, stream=None)
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
+    spec_accept_lazy(logits, drafts, accept_len, out_tokens, num_drafts=None, seq_lens_inout=None, status=None,
+                     stream=None)
     sdva_status_string(code)
 """
 from __future__ import annotations
@@ -38,6 +40,8 @@ STATUS_BAD_PAGE = 1
 STATUS_OVERFLOW = 2
 STATUS_BAD_DRAFT = 4
 STATUS_TIMEOUT = 8
+STATUS_BAD_COUNT = 16
+LAZY_WALK_MIN_LANES = 48  # SDVA_LAZY_WALK_MIN_LANES: spec_accept_lazy walks rows from this many lanes on
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -75,11 +79,13 @@ _lib.verify_attn_noalloc.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I,
                                      _P, _P, _P]
 _lib.spec_accept.restype = _I
 _lib.spec_accept.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+_lib.spec_accept_lazy.restype = _I
+_lib.spec_accept_lazy.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
-            "sdva_status_string")
+            "spec_accept_lazy", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -217,6 +223,23 @@ def spec_accept(logits: torch.Tensor, drafts: torch.Tensor | None, accept_len: t
                           _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"), _dptr(status, torch.int32, "status"),
                           _stream(stream))
     _check("spec_accept", rc)
+
+
+def spec_accept_lazy(logits: torch.Tensor, drafts: torch.Tensor | None, accept_len: torch.Tensor,
+                     out_tokens: torch.Tensor, num_drafts: torch.Tensor | None = None,
+                     seq_lens_inout: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """As spec_accept, reading each lane's rows only up to its first disagreement;
+    num_drafts int32 [B] (None: W-1 each); out_tokens is -1 after row accept_len."""
+    B, W, V = logits.shape
+    rc = _lib.spec_accept_lazy(_dptr(logits, torch.float32, "logits"), B, W, V,
+                               _dptr(drafts, torch.int32, "drafts") if W > 1 else None,
+                               _dptr(num_drafts, torch.int32, "num_drafts"),
+                               _dptr(accept_len, torch.int32, "accept_len"),
+                               _dptr(out_tokens, torch.int32, "out_tokens"),
+                               _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"),
+                               _dptr(status, torch.int32, "status"), _stream(stream))
+    _check("spec_accept_lazy", rc)
 
 
 def raw_library() -> ctypes.CDLL:

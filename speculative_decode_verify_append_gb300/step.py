@@ -12,7 +12,7 @@ import math
 
 import torch
 
-from . import (KVCache, kv_append_quant, spec_accept, verify_attn, verify_attn_workspace_size)
+from . import (KVCache, kv_append_quant, spec_accept, spec_accept_lazy, verify_attn, verify_attn_workspace_size)
 
 
 class VerifyStep:
@@ -39,6 +39,11 @@ class VerifyStep:
 
     def accept(self, logits, drafts, seq_lens_inout=None, stream=None):
         spec_accept(logits, drafts, self.accept_len, self.out_tokens, seq_lens_inout, self.status, stream)
+
+    def accept_lazy(self, logits, drafts, num_drafts=None, seq_lens_inout=None, stream=None):
+        """Acceptance reading each lane's rows only up to its first disagreement."""
+        spec_accept_lazy(logits, drafts, self.accept_len, self.out_tokens, num_drafts, seq_lens_inout, self.status,
+                         stream)
 
     def run(self, cache: KVCache, q, k_win, v_win, page_table, seq_lens, logits=None, drafts=None,
             commit: bool = True, stream=None):

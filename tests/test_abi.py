@@ -74,7 +74,7 @@ def test_status_strings(lib):
     f = lib.sdva_status_string
     f.restype = ctypes.c_char_p
     f.argtypes = [ctypes.c_int]
-    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 3, -99):
+    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 16, 3, -99):
         s = f(code)
         assert s and len(s) >= 2
 
@@ -119,3 +119,20 @@ def test_argument_validation_returns_before_cuda(lib):
     assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
     assert sa(fake, 0, 4, 100, fake, fake, fake, None, None, None) == -1
     assert sa(fake, 1, 17, 100, fake, fake, fake, None, None, None) == -2
+    lz = lib.spec_accept_lazy
+    lz.restype = ctypes.c_int
+    assert lz(fake, 1, 4, 100, None, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
+    assert lz(fake, 1, 4, 0, fake, None, fake, fake, None, None, None) == -1
+    assert lz(fake, 1, 4, 100, fake, None, None, fake, None, None, None) == -1
+    assert lz(fake, 1, 17, 100, fake, fake, fake, fake, None, None, None) == -2
+    assert lz(fake, 5000, 16, 100, fake, fake, fake, fake, None, None, None) == -2  # more than 65535 rows
+
+
+def test_header_constants_match_the_binding(lib):
+    text = open(os.path.join(ROOT, "include", "sdva.h")).read()
+    defs = dict(re.findall(r"#define (SDVA_\w+) \(?(-?\d+)\)?", text))
+    import speculative_decode_verify_append_gb300 as sdva
+    assert int(defs["SDVA_LAZY_WALK_MIN_LANES"]) == sdva.LAZY_WALK_MIN_LANES
+    assert int(defs["SDVA_STATUS_BAD_COUNT"]) == sdva.STATUS_BAD_COUNT
+    assert int(defs["SDVA_STATUS_BAD_DRAFT"]) == sdva.STATUS_BAD_DRAFT
+    assert int(defs["SDVA_ERR_WORKSPACE"]) == sdva.ERR_WORKSPACE
