@@ -168,6 +168,28 @@ def append(cache: Cache, k_new_bf16: np.ndarray, v_new_bf16: np.ndarray, page_ta
     return int(st[0])
 
 
+def append_ragged(cache: Cache, k_new_bf16: np.ndarray, v_new_bf16: np.ndarray, page_table: np.ndarray,
+                  seq_lens: np.ndarray, n_lane: np.ndarray) -> int:
+    """Per-lane token counts: lane b writes only its first n_lane[b] tokens
+    (0 <= n_lane[b] <= n_new), i.e. exactly what appending that lane's
+    truncated window on its own writes; a lane with no token is not examined.
+    A count outside [0, n_new] sets status bit 16 and leaves the lane alone.
+    Returns the OR of the status bits."""
+    k = _as(k_new_bf16, np.uint16)
+    v = _as(v_new_bf16, np.uint16)
+    pt = _as(page_table, np.int32)
+    sl = _as(seq_lens, np.int32)
+    n_new = k.shape[1]
+    st = 0
+    for b in range(k.shape[0]):
+        n = int(n_lane[b])
+        if n < 0 or n > n_new:
+            st |= 16
+        elif n > 0:
+            st |= append(cache, k[b:b + 1, :n], v[b:b + 1, :n], pt[b:b + 1], sl[b:b + 1])
+    return st
+
+
 def verify_attn(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
                 sm_scale: float, rows=None, threads: int = 1) -> tuple[np.ndarray, int]:
     """fp64 attention of every window row over its visible keys.

@@ -138,3 +138,87 @@ def test_overflow_and_bad_page_are_flagged_and_skipped():
     assert oracle.append(cache, k, k, bad, np.array([62], np.int32)) == 1
     assert (cache.k_codes == before).all()
     assert oracle.append(cache, k, k, table, np.array([-1], np.int32)) == 2
+
+
+# ---- per-lane token counts (a padded window whose lanes drafted different numbers of tokens) ----
+
+def _ragged_history(dtype, seed, steps=6, W=6, lanes=3, H=2):
+    rng = np.random.default_rng(seed)
+    L = np.array([5, 62, 0][:lanes], np.int32)
+    need = (int(L.max()) + steps * W + W + PAGE - 1) // PAGE
+    table = rng.permutation(need * lanes).astype(np.int32).reshape(lanes, need)
+    cache = oracle.Cache(dtype, need * lanes, H)
+    bc = brute.Cache(dtype)
+    for b in range(lanes):  # the lanes' starting context
+        if L[b]:
+            k = synth.normal_bf16(rng, (1, int(L[b]), H, 128))
+            assert oracle.append(cache, k, k, table[b:b + 1], np.zeros(1, np.int32)) == 0
+            brute.append(bc, _rows(k, k, 0), list(table[b]), 0)
+    written = L.copy()
+    for s in range(steps):
+        k = synth.normal_bf16(rng, (lanes, W, H, 128))
+        v = synth.normal_bf16(rng, (lanes, W, H, 128))
+        if s == 2:
+            k[1, 0, 1, 9] = synth.to_bf16_bits(np.array([70.0], np.float32))[0]  # forces a scale growth
+        n = rng.integers(0, W + 1, size=lanes).astype(np.int32)
+        assert oracle.append_ragged(cache, k, v, table, L, n) == 0
+        for b in range(lanes):
+            if n[b]:
+                brute.append(bc, _rows(k[:, :n[b]], v[:, :n[b]], b), list(table[b]), int(L[b]))
+        written = np.maximum(written, L + n)
+        L = L + rng.integers(0, n + 1).astype(np.int32)
+    return cache, bc, table, written
+
+
+@pytest.mark.parametrize("dtype", [oracle.KV_FP8, oracle.KV_INT4])
+def test_ragged_append_matches_brute(dtype):
+    cache, bc, table, written = _ragged_history(dtype, 31)
+    _compare(cache, bc, dtype, table, written)
+
+
+@pytest.mark.parametrize("dtype", [oracle.KV_FP8, oracle.KV_INT4])
+def test_ragged_with_full_counts_is_the_plain_append(dtype):
+    rng = np.random.default_rng(32)
+    B, W, H = 3, 7, 2
+    table = rng.permutation(4 * B).astype(np.int32).reshape(B, 4)
+    L = np.array([10, 63, 120], np.int32)
+    k = synth.normal_bf16(rng, (B, W, H, 128))
+    v = synth.normal_bf16(rng, (B, W, H, 128))
+    a, b = oracle.Cache(dtype, 4 * B, H), oracle.Cache(dtype, 4 * B, H)
+    assert oracle.append(a, k, v, table, L) == 0
+    assert oracle.append_ragged(b, k, v, table, L, np.full(B, W, np.int32)) == 0
+    for n in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert np.array_equal(getattr(a, n), getattr(b, n)), n
+
+
+def test_ragged_int4_in_two_parts_equals_one_append():
+    # INT4 scales belong to single tokens, so writing a window in two parts changes nothing
+    rng = np.random.default_rng(33)
+    B, W, H = 2, 9, 3
+    table = rng.permutation(3 * B).astype(np.int32).reshape(B, 3)
+    L = np.array([60, 3], np.int32)
+    k = synth.normal_bf16(rng, (B, W, H, 128))
+    v = synth.normal_bf16(rng, (B, W, H, 128))
+    whole, parts = oracle.Cache(oracle.KV_INT4, 3 * B, H), oracle.Cache(oracle.KV_INT4, 3 * B, H)
+    assert oracle.append(whole, k, v, table, L) == 0
+    n1 = np.array([4, 0], np.int32)
+    assert oracle.append_ragged(parts, k, v, table, L, n1) == 0
+    rest_k = np.stack([np.roll(k[b], -n1[b], axis=0) for b in range(B)])
+    rest_v = np.stack([np.roll(v[b], -n1[b], axis=0) for b in range(B)])
+    assert oracle.append_ragged(parts, rest_k, rest_v, table, L + n1, W - n1) == 0
+    for n in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert np.array_equal(getattr(whole, n), getattr(parts, n)), n
+
+
+def test_ragged_invalid_and_empty_counts():
+    rng = np.random.default_rng(34)
+    B, W, H = 3, 4, 1
+    table = np.array([[0, 1], [2, 3], [-5, 4]], np.int32)  # lane 2 has a bad page id
+    L = np.array([0, 10, 0], np.int32)
+    k = synth.normal_bf16(rng, (B, W, H, 128))
+    c = oracle.Cache(oracle.KV_FP8, 5, H)
+    st = oracle.append_ragged(c, k, k, table, L, np.array([W + 1, -1, 0], np.int32))
+    assert st == 16  # lane 2 writes nothing, so its bad page is never examined
+    assert not c.k_codes.any() and not c.k_scales.any()
+    assert oracle.append_ragged(c, k, k, table, L, np.array([2, 0, 1], np.int32)) == 1
+    assert c.k_codes[0, 0, :2].any() and not c.k_codes[0, 0, 2:].any()
