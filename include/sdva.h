@@ -14,6 +14,7 @@
  *
  * This library implements the three data-parallel calls of that step:
  *   kv_append_quant  -- write new K/V rows into the quantised, paged cache
+ *   kv_append_quant_ragged -- the same with a token count per lane
  *   verify_attn      -- batched, causal-in-window, GQA attention of every
  *                       lane's window over its whole cached context
  *   spec_accept      -- argmax per window position, longest agreeing draft
@@ -106,7 +107,7 @@ typedef struct {
 #define SDVA_STATUS_OVERFLOW 2  /* L_b < 0, or L_b + n does not fit the lane's row / max_context */
 #define SDVA_STATUS_BAD_DRAFT 4 /* a draft id is outside [0, vocab) */
 #define SDVA_STATUS_TIMEOUT 8   /* a bounded device wait gave up */
-#define SDVA_STATUS_BAD_COUNT 16 /* a per-lane draft count is outside [0, window - 1] */
+#define SDVA_STATUS_BAD_COUNT 16 /* a per-lane draft or token count is out of range */
 
 /*
  * kv_append_quant -- write tokens [L_b, L_b + n_new) of every lane into the
@@ -126,6 +127,24 @@ typedef struct {
 int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes, int n_new,
                     const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens, int32_t* status,
                     sdva_stream_t stream);
+
+/*
+ * kv_append_quant_ragged -- kv_append_quant with a token count per lane, for a
+ * padded window whose lanes drafted different numbers of tokens (the draft
+ * count is chosen per workload: NInfer review, section "아키텍처 ③").
+ *   n_lane: int32 [num_lanes] (device, required): lane b writes only its
+ *           first n_lane[b] tokens, positions [L_b, L_b + n_lane[b]); the
+ *           rest of its n_new input rows are not read.  The result is what
+ *           appending each lane's truncated window on its own writes, so
+ *           padding never touches the cache or an FP8 page scale.
+ * A lane with n_lane[b] == 0 is not examined.  A count outside [0, n_new]
+ * sets SDVA_STATUS_BAD_COUNT and skips the lane; the other rules, layouts
+ * and return codes are those of kv_append_quant (the range and page checks
+ * apply to [L_b, L_b + n_lane[b])).
+ */
+int kv_append_quant_ragged(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes,
+                           int n_new, const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
+                           const int32_t* seq_lens, int32_t* status, sdva_stream_t stream);
 
 /*
  * verify_attn_workspace_size -- bytes of device scratch verify_attn needs for

@@ -8,6 +8,7 @@ raises.  PyTorch supplies device memory and streams.
 The calls mirror ``include/sdva.h``:
 
     kv_append_quant(cache, k_new, v_new, page_table, seq_lens, status=None, stream=None)
+    kv_append_quant_ragged(cache, k_new, v_new, n_lane, page_table, seq_lens, status=None, stream=None)
     verify_attn_workspace_size(num_lanes, window, num_q_heads, num_kv_heads, max_context, num_sms=0)
     verify_attn(cache, q, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None, stream=None)
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
@@ -69,6 +70,8 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _lib.kv_append_quant.restype = _I
 _lib.kv_append_quant.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _P, _I, _I, _P, _I, _P, _P, _P]
+_lib.kv_append_quant_ragged.restype = _I
+_lib.kv_append_quant_ragged.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _P, _I, _I, _P, _P, _I, _P, _P, _P]
 _lib.verify_attn_workspace_size.restype = ctypes.c_size_t
 _lib.verify_attn_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
 _lib.verify_attn.restype = _I
@@ -84,7 +87,7 @@ _lib.spec_accept_lazy.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
-EXPORTED = ("kv_append_quant", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
+EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
             "spec_accept_lazy", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -174,6 +177,23 @@ def kv_append_quant(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pa
                               _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(status, torch.int32, "status"),
                               _stream(stream))
     _check("kv_append_quant", rc)
+
+
+def kv_append_quant_ragged(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, n_lane: torch.Tensor,
+                           page_table: torch.Tensor, seq_lens: torch.Tensor, status: torch.Tensor | None = None,
+                           stream=None) -> None:
+    """As kv_append_quant; lane b writes only its first n_lane[b] tokens (int32 [B] on the device)."""
+    B, n_new = k_new.shape[0], k_new.shape[1]
+    if n_lane is None:
+        raise ValueError("n_lane is required")
+    s = cache.struct()
+    rc = _lib.kv_append_quant_ragged(ctypes.byref(s), _dptr(k_new, torch.bfloat16, "k_new"),
+                                     _dptr(v_new, torch.bfloat16, "v_new"), B, n_new,
+                                     _dptr(n_lane, torch.int32, "n_lane"),
+                                     _dptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                                     _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(status, torch.int32, "status"),
+                                     _stream(stream))
+    _check("kv_append_quant_ragged", rc)
 
 
 def verify_attn_workspace_size(num_lanes: int, window: int, num_q_heads: int, num_kv_heads: int, max_context: int,

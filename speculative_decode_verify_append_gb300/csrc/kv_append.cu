@@ -28,19 +28,33 @@ struct AppendArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   int32_t* status;
+  const int32_t* n_lane;  // nullable [B]: tokens lane b writes (<= n_new); NULL: n_new each
   int num_pages, num_kv_heads, n_new, max_pages;
 };
 
 constexpr int kAppendThreads = 256;
 
-// Lane admission shared by both kernels: the whole token range must fit the
-// lane's page-table row and every touched page id must be valid; otherwise
-// the lane is skipped and flagged (once, by the lane's first CTA).
-__device__ bool lane_admitted(const AppendArgs& a, int b, int L, bool report) {
+// Tokens lane b writes: its own count when per-lane counts are given (a
+// padded window whose lanes drafted different numbers of tokens), else n_new.
+// A count outside [0, n_new] skips the lane and is flagged (once).
+__device__ __forceinline__ int lane_tokens(const AppendArgs& a, int b, bool report) {
+  if (a.n_lane == nullptr) return a.n_new;
+  const int n = a.n_lane[b];
+  if (n < 0 || n > a.n_new) {
+    if (report && threadIdx.x == 0) raise_status(a.status, SDVA_STATUS_BAD_COUNT);
+    return 0;
+  }
+  return n;
+}
+
+// Lane admission shared by both kernels: the lane's token range [L, L + n)
+// must fit its page-table row and every touched page id must be valid;
+// otherwise the lane is skipped and flagged (once, by the lane's first CTA).
+__device__ bool lane_admitted(const AppendArgs& a, int b, int L, int n, bool report) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  const long long end = (long long)L + a.n_new;
+  const long long end = (long long)L + n;
   if (L < 0 || end > (long long)a.max_pages * kPage) {
     if (report && threadIdx.x == 0) raise_status(a.status, SDVA_STATUS_OVERFLOW);
     return false;
@@ -73,12 +87,15 @@ __device__ __forceinline__ float block_max(float v) {
 __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a) {
   const int slot = blockIdx.x, b = blockIdx.y;
   const int hk = blockIdx.z >> 1, is_v = blockIdx.z & 1;
+  const bool report = slot == 0 && blockIdx.z == 0;
+  const int n = lane_tokens(a, b, report);
+  if (n == 0) return;  // nothing to write: the lane is not examined
   const int L = a.seq_lens[b];
-  if (!lane_admitted(a, b, L, slot == 0 && blockIdx.z == 0)) return;
+  if (!lane_admitted(a, b, L, n, report)) return;
   const int lp = L / kPage + slot;
-  if ((long long)lp * kPage >= (long long)L + a.n_new) return;
+  if ((long long)lp * kPage >= (long long)L + n) return;
   const int pid = a.page_table[(size_t)b * a.max_pages + lp];
-  const int t0 = max(L, lp * kPage), t1 = min(L + a.n_new, lp * kPage + kPage);
+  const int t0 = max(L, lp * kPage), t1 = min(L + n, lp * kPage + kPage);
   const int start = t0 - lp * kPage, count = t1 - t0;
   const size_t token_stride = (size_t)a.num_kv_heads * kHeadDim;
   const uint16_t* src = (is_v ? a.v_new : a.k_new) + ((size_t)b * a.n_new + (t0 - L)) * token_stride +
@@ -143,12 +160,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a
 // group of 32 dims): 64 bytes in, 16 bytes of codes and one fp16 scale out.
 __global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs a) {
   const int slot = blockIdx.x, b = blockIdx.y;
+  const int n = lane_tokens(a, b, slot == 0);
+  if (n == 0) return;  // nothing to write: the lane is not examined
   const int L = a.seq_lens[b];
-  if (!lane_admitted(a, b, L, slot == 0)) return;
+  if (!lane_admitted(a, b, L, n, slot == 0)) return;
   const int lp = L / kPage + slot;
-  if ((long long)lp * kPage >= (long long)L + a.n_new) return;
+  if ((long long)lp * kPage >= (long long)L + n) return;
   const int pid = a.page_table[(size_t)b * a.max_pages + lp];
-  const int t0 = max(L, lp * kPage), t1 = min(L + a.n_new, lp * kPage + kPage);
+  const int t0 = max(L, lp * kPage), t1 = min(L + n, lp * kPage + kPage);
   const int count = t1 - t0;
   const int H = a.num_kv_heads;
   const size_t token_stride = (size_t)H * kHeadDim;
@@ -196,9 +215,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs 
 
 using namespace sdva;
 
-extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes,
-                               int n_new, const int32_t* page_table, int max_pages_per_lane,
-                               const int32_t* seq_lens, int32_t* status, sdva_stream_t stream) {
+namespace {
+int append_impl(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes, int n_new,
+                const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
+                int32_t* status, sdva_stream_t stream) {
   if (cache == nullptr || k_new == nullptr || v_new == nullptr || page_table == nullptr || seq_lens == nullptr)
     return SDVA_ERR_INVALID;
   if (cache->k_codes == nullptr || cache->v_codes == nullptr || cache->k_scales == nullptr ||
@@ -220,6 +240,7 @@ extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, co
   a.page_table = page_table;
   a.seq_lens = seq_lens;
   a.status = status;
+  a.n_lane = n_lane;
   a.num_pages = cache->num_pages;
   a.num_kv_heads = cache->num_kv_heads;
   a.n_new = n_new;
@@ -232,4 +253,21 @@ extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, co
     append_int4_kernel<<<dim3(slots, num_lanes), kAppendThreads, 0, s>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes,
+                               int n_new, const int32_t* page_table, int max_pages_per_lane,
+                               const int32_t* seq_lens, int32_t* status, sdva_stream_t stream) {
+  return append_impl(cache, k_new, v_new, num_lanes, n_new, nullptr, page_table, max_pages_per_lane, seq_lens,
+                     status, stream);
+}
+
+extern "C" int kv_append_quant_ragged(const sdva_kv_cache* cache, const void* k_new, const void* v_new,
+                                      int num_lanes, int n_new, const int32_t* n_lane, const int32_t* page_table,
+                                      int max_pages_per_lane, const int32_t* seq_lens, int32_t* status,
+                                      sdva_stream_t stream) {
+  if (n_lane == nullptr) return SDVA_ERR_INVALID;
+  return append_impl(cache, k_new, v_new, num_lanes, n_new, n_lane, page_table, max_pages_per_lane, seq_lens,
+                     status, stream);
 }

@@ -22,7 +22,7 @@ extern "C" const char* sdva_status_string(int code) {
     case SDVA_STATUS_TIMEOUT:
       return "device status: a bounded device wait timed out";
     case SDVA_STATUS_BAD_COUNT:
-      return "device status: a per-lane draft count is outside [0, window - 1]";
+      return "device status: a per-lane draft or token count is out of range";
     default:
       return code > 0 ? "device status: several bits set" : "unknown code";
   }

@@ -12,7 +12,8 @@ import math
 
 import torch
 
-from . import (KVCache, kv_append_quant, spec_accept, spec_accept_lazy, verify_attn, verify_attn_workspace_size)
+from . import (KVCache, kv_append_quant, kv_append_quant_ragged, spec_accept, spec_accept_lazy, verify_attn,
+               verify_attn_workspace_size)
 
 
 class VerifyStep:
@@ -32,6 +33,10 @@ class VerifyStep:
 
     def append(self, cache: KVCache, k_win, v_win, page_table, seq_lens, stream=None):
         kv_append_quant(cache, k_win, v_win, page_table, seq_lens, self.status, stream)
+
+    def append_ragged(self, cache: KVCache, k_win, v_win, n_lane, page_table, seq_lens, stream=None):
+        """Lane b appends only its first n_lane[b] window tokens (its own 1 + d_b)."""
+        kv_append_quant_ragged(cache, k_win, v_win, n_lane, page_table, seq_lens, self.status, stream)
 
     def attend(self, cache: KVCache, q, page_table, seq_lens, stream=None):
         verify_attn(cache, q, page_table, seq_lens, self.max_context, self.sm_scale, self.out, self.workspace,

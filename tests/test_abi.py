@@ -89,6 +89,10 @@ def test_argument_validation_returns_before_cuda(lib):
     P = ctypes.c_void_p
     fake = P(0x1000)  # never dereferenced: every call below fails validation first
     c = _Cache(0, 4, 64, 1, 128, fake, fake, fake, fake)
+    rag = lib.kv_append_quant_ragged
+    rag.restype = ctypes.c_int
+    assert rag(ctypes.byref(c), fake, fake, 1, 1, None, fake, 1, fake, None, None) == -1  # counts required
+    assert rag(ctypes.byref(c), fake, fake, 1, 0, fake, fake, 1, fake, None, None) == -1
     app = lib.kv_append_quant
     app.restype = ctypes.c_int
     assert app(ctypes.byref(c), None, fake, 1, 1, fake, 1, fake, None, None) == -1

@@ -162,3 +162,59 @@ def test_host_argument_errors():
     with pytest.raises(sdva.SdvaError) as e:
         sdva.kv_append_quant(gcache, k[:, :0], k[:, :0], t, i32_dev(np.zeros(1)))
     assert e.value.code == sdva.ERR_INVALID
+
+
+# ---- per-lane token counts -------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+def test_ragged_append_history_parity(dtype):
+    sdva = _sdva()
+    rng = np.random.default_rng(77 + dtype)
+    B, W, H, steps = 5, 16, 4, 8
+    L = np.array([0, 5, 63, 64, 130], np.int32)
+    need = (int(L.max()) + steps * W + W + PAGE - 1) // PAGE
+    table = rng.permutation(need * B).astype(np.int32).reshape(B, need)
+    gcache = sdva.KVCache(dtype, need * B, H)
+    ocache = oracle.Cache(dtype, need * B, H)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tdev = i32_dev(table)
+    for b in range(B):  # starting context, one plain append per lane
+        if L[b]:
+            k = synth.normal_bf16(rng, (1, int(L[b]), H, 128))
+            sdva.kv_append_quant(gcache, bf16_dev(k), bf16_dev(k), tdev[b:b + 1], i32_dev(np.zeros(1)), st)
+            assert oracle.append(ocache, k, k, table[b:b + 1], np.zeros(1, np.int32)) == 0
+    for s in range(steps):
+        k = synth.normal_bf16(rng, (B, W, H, 128))
+        v = synth.normal_bf16(rng, (B, W, H, 128))
+        if s == 3:  # padding past lane 1's count is huge: it must not reach the page scale
+            k[1, 2:, :, :] = synth.to_bf16_bits(np.array([3.0e4], np.float32))[0]
+        if s == 5:  # a large token inside lane 2's count forces a growth re-encode
+            v[2, 0, 3, 11] = synth.to_bf16_bits(np.array([-500.0], np.float32))[0]
+        n = rng.integers(0, W + 1, size=B).astype(np.int32)
+        n[s % B] = 0
+        n[(s + 1) % B] = W
+        if s == 3:
+            n[1] = 2
+        sdva.kv_append_quant_ragged(gcache, bf16_dev(k), bf16_dev(v), i32_dev(n), tdev, i32_dev(L), st)
+        assert oracle.append_ragged(ocache, k, v, table, L, n) == 0
+        L = L + rng.integers(0, n + 1).astype(np.int32)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _assert_cache_equal(gcache, ocache, "ragged history")
+
+
+def test_ragged_invalid_and_empty_counts():
+    sdva = _sdva()
+    rng = np.random.default_rng(78)
+    B, W, H = 3, 4, 1
+    table = np.array([[0, 1], [2, 3], [-5, 4]], np.int32)  # lane 2 has a bad page id
+    L = np.array([0, 10, 0], np.int32)
+    k = synth.normal_bf16(rng, (B, W, H, 128))
+    gcache = sdva.KVCache(synth.KV_FP8, 5, H)
+    ocache = oracle.Cache(synth.KV_FP8, 5, H)
+    for n in (np.array([W + 1, -1, 0], np.int32), np.array([2, 0, 1], np.int32)):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdva.kv_append_quant_ragged(gcache, bf16_dev(k), bf16_dev(k), i32_dev(n), i32_dev(table), i32_dev(L), st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == oracle.append_ragged(ocache, k, k, table, L, n)
+        _assert_cache_equal(gcache, ocache, f"counts {n.tolist()}")

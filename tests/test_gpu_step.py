@@ -55,6 +55,59 @@ def test_multi_step_loop_matches_oracle(dtype):
     assert np.array_equal(g["k_codes"], ocache.k_codes) and np.array_equal(g["v_codes"], ocache.v_codes)
 
 
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+def test_ragged_step_loop_matches_oracle(dtype):
+    """Lanes with their own draft counts d_b in one padded window: the ragged
+    append writes 1 + d_b tokens per lane, verify rows 0 .. d_b are compared,
+    and the lazy acceptance uses the same counts."""
+    sdva, VerifyStep = _sdva()
+    W, Hq, Hkv, V = 8, 12, 2, 3000
+    lens = np.array([70, 640, 1333, 5], np.int32)
+    B, steps = len(lens), 5
+    spec = synth.Spec("ragged", 12, B, 0, 0, Hq, Hkv, W, dtype, V, 0.8, True)
+    table, total = synth.page_table_for(spec, lens + steps * W, W)
+    step0 = synth.make_step(spec, seq_lens=lens, with_accept=False)
+    step0.page_table, step0.num_pages = table, total
+    # the starting contexts (every window, step 0's included, goes through the ragged append)
+    gcache = sdva.KVCache(dtype, total, Hkv)
+    ocache = oracle.Cache(dtype, total, Hkv)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tdev = i32_dev(table)
+    for b, L in enumerate(lens):
+        for start, n in synth.fill_chunks(int(L), 256):
+            k, v = synth.context_chunk(spec, b, start, n)
+            sdva.kv_append_quant(gcache, bf16_dev(k[None]), bf16_dev(v[None]), tdev[b:b + 1],
+                                 i32_dev(np.array([start])), st)
+            assert oracle.append(ocache, k[None], v[None], table[b:b + 1], np.array([start], np.int32)) == 0
+    vs = VerifyStep(B, W, Hq, Hkv, int(lens.max()) + steps * W, V)
+    rng = np.random.default_rng(13)
+    L_host, L_dev = lens.copy(), i32_dev(lens)
+    for s in range(steps):
+        stp = synth.make_step(spec, seq_lens=L_host, tag=f"r{s}")
+        d = rng.integers(0, W, size=B).astype(np.int32)
+        d[s % B] = W - 1
+        d[(s + 2) % B] = 0
+        vs.append_ragged(gcache, bf16_dev(stp.k_win), bf16_dev(stp.v_win), i32_dev(d + 1), tdev, L_dev)
+        assert oracle.append_ragged(ocache, stp.k_win, stp.v_win, table, L_host, d + 1) == 0
+        vs.attend(gcache, bf16_dev(stp.q), tdev, L_dev)
+        vs.accept_lazy(torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts), i32_dev(d), L_dev)
+        torch.cuda.synchronize()
+        want, _ = oracle.verify_attn(ocache, stp.q, table, L_host, SM_SCALE, threads=8)
+        got = vs.out.float().cpu().numpy()
+        for b in range(B):  # rows past a lane's count attend to padding: not compared
+            assert_close(got[b, :d[b] + 1], want[b, :d[b] + 1], f"step {s} lane {b}")
+        acc, tok, newL, _ = oracle.spec_accept_lazy(stp.logits, stp.drafts, d, L_host)
+        assert np.array_equal(vs.accept_len.cpu().numpy(), acc)
+        assert np.array_equal(vs.out_tokens.cpu().numpy(), tok)
+        assert np.array_equal(L_dev.cpu().numpy(), newL)
+        L_host = newL
+    assert int(vs.status.item()) == 0
+    for n in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        g = getattr(gcache, n).cpu().numpy()
+        w = getattr(ocache, n)
+        assert np.array_equal(g.view(np.uint8), w.view(np.uint8)), n
+
+
 def test_cuda_graph_replay_matches_eager():
     sdva, VerifyStep = _sdva()
     spec = synth.WORKLOADS["multi_lane"]
