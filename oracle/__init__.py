@@ -74,6 +74,8 @@ def _load():
             lib.oracle_spec_accept.argtypes = [P, I, I, I, P, P, P, P, P]
             lib.oracle_spec_accept_lazy.restype = I
             lib.oracle_spec_accept_lazy.argtypes = [P, I, I, I, P, P, P, P, P, P]
+            lib.oracle_spec_accept_sampled.restype = I
+            lib.oracle_spec_accept_sampled.argtypes = [P, P, I, I, I, P, P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -259,4 +261,27 @@ def spec_accept_lazy(logits: np.ndarray, drafts: np.ndarray, num_drafts: np.ndar
     st = np.zeros(1, np.int32)
     _load().oracle_spec_accept_lazy(_ptr(lg), B, W, V, _ptr(dr) if dr.size else None, _ptr(nd), _ptr(acc),
                                     _ptr(tok), _ptr(sl), _ptr(st))
+    return acc, tok, sl, int(st[0])
+
+
+def spec_accept_sampled(logits: np.ndarray, draft_probs: np.ndarray, drafts: np.ndarray, u_accept: np.ndarray,
+                        u_sample: np.ndarray, seq_lens: np.ndarray | None = None):
+    """Lossless stochastic acceptance.  logits [B][W][V], draft_probs [B][W-1][V],
+    drafts [B][W-1], u_accept [B][W-1], u_sample [B] (uniforms in [0, 1)).
+    Returns (accept_len [B], out_tokens [B][W]: drafts, the drawn token, -1 after;
+    new seq_lens or None, status)."""
+    lg = _as(logits, np.float32)
+    B, W, V = lg.shape
+    q = _as(draft_probs, np.float32).reshape(B, W - 1, V) if W > 1 else np.zeros((B, 0, V), np.float32)
+    dr = _as(drafts, np.int32).reshape(B, W - 1) if W > 1 else np.zeros((B, 0), np.int32)
+    ua = _as(u_accept, np.float32).reshape(B, W - 1) if W > 1 else np.zeros((B, 0), np.float32)
+    us = _as(u_sample, np.float32).reshape(B)
+    acc = np.zeros(B, np.int32)
+    tok = np.zeros((B, W), np.int32)
+    sl = None if seq_lens is None else _as(seq_lens, np.int32).copy()
+    st = np.zeros(1, np.int32)
+    rc = _load().oracle_spec_accept_sampled(_ptr(lg), _ptr(q) if q.size else None, B, W, V,
+                                            _ptr(dr) if dr.size else None, _ptr(ua) if ua.size else None, _ptr(us),
+                                            _ptr(acc), _ptr(tok), _ptr(sl), _ptr(st))
+    assert rc == 0
     return acc, tok, sl, int(st[0])

@@ -189,3 +189,40 @@ def accept_lazy(logits_rows, drafts, d):
     t = [argmax(r) for r in logits_rows]
     a = max(k for k in range(d + 1) if all(drafts[i] == t[i] for i in range(k)))
     return a, t[:a + 1] + [-1] * (len(logits_rows) - a - 1)
+
+
+def accept_sampled(logits_rows, q_rows, drafts, u_accept, u_sample):
+    """Lossless stochastic acceptance restated with exact sums: the ratio test
+    u < p(x) / q(x) (a zero q accepts), the residual max(0, p - q), and the
+    inverse CDF through exactly rounded prefix sums.  Returns (a, tokens)."""
+    import math
+
+    def softmax(row):
+        m = max(row)
+        e = [math.exp(v - m) for v in row]
+        s = math.fsum(e)
+        return [v / s for v in e]
+
+    d = len(drafts)
+    n = len(logits_rows[0])
+    a = d
+    for i in range(d):
+        x = drafts[i]
+        if not 0 <= x < n:
+            a = i
+            break
+        p = softmax(logits_rows[i])
+        q = q_rows[i][x]
+        if not (q == 0.0 or u_accept[i] < p[x] / q):
+            a = i
+            break
+    p = softmax(logits_rows[a])
+    w = [max(0.0, p[x] - q_rows[a][x]) for x in range(n)] if a < d else p
+    if math.fsum(w) <= 0.0:
+        w = p
+    z = math.fsum(w)
+    target = u_sample * z
+    k = next((x for x in range(n) if math.fsum(w[:x + 1]) > target), None)
+    if k is None:
+        k = max(x for x in range(n) if w[x] > 0.0)
+    return a, list(drafts[:a]) + [k] + [-1] * (len(logits_rows) - a - 1)

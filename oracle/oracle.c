@@ -47,6 +47,15 @@
  *      drafts only drafts[b][0 .. d_b) are compared, and the rows after the
  *      first disagreement decide nothing, so the lazy form reports argmaxes
  *      only for rows 0 .. a and -1 after them.
+ *   R8 Lossless stochastic acceptance (DFlash2 keeps the draft model's
+ *      conditional distribution q: NInfer review, section "아키텍처 ③"):
+ *      p_i = softmax(logits row i) (temperature 1); draft i is accepted when
+ *      u_i * q_i(x_i) < p_i(x_i); at the first rejection a, one token is drawn
+ *      from max(0, p_a - q_a) normalised (from p_d when every draft is
+ *      accepted) by the inverse CDF in index order at u_sample * Z: the
+ *      smallest k whose running sum exceeds it, else the last k of positive
+ *      weight; a residual of zero mass falls back to p_a.  The uniforms are
+ *      inputs.  An out-of-vocabulary draft is a rejection and sets a status bit.
  *
  * Arithmetic: codecs in IEEE fp32 exactly as stated (compiled with
  * -ffp-contract=off, no fast-math); attention in fp64, two-pass softmax.
@@ -625,5 +634,92 @@ int oracle_spec_accept_lazy(const float* logits, int num_lanes, int window, int 
         if (seq_lens_inout)
             seq_lens_inout[b] += 1 + a;
     }
+    return 0;
+}
+
+/* Lossless stochastic acceptance (R8).  logits [B][W][V]; draft_probs
+ * [B][W-1][V] (row i: the draft distribution q_i that drafts[b][i] was drawn
+ * from); u_accept [B][W-1] and u_sample [B] uniforms in [0, 1).  Outputs as
+ * for the lazy form: out_tokens = drafts[0 .. a), the drawn token at a, -1
+ * after; accept_len = a; the commit adds 1 + a. */
+static void softmax_row(const float* l, int n, double* p)
+{
+    double m = l[0], s = 0.0;
+    int x;
+    for (x = 1; x < n; ++x)
+        if (l[x] > m)
+            m = l[x];
+    for (x = 0; x < n; ++x) {
+        p[x] = exp((double)l[x] - m);
+        s += p[x];
+    }
+    for (x = 0; x < n; ++x)
+        p[x] /= s;
+}
+
+int oracle_spec_accept_sampled(const float* logits, const float* draft_probs, int num_lanes, int window, int vocab,
+                               const int32_t* drafts, const float* u_accept, const float* u_sample,
+                               int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout, int32_t* status)
+{
+    int b, i, x, d = window - 1;
+    double* p = malloc(sizeof(double) * (size_t)vocab);
+    double* w = malloc(sizeof(double) * (size_t)vocab);
+    if (!p || !w) {
+        free(p);
+        free(w);
+        return -1;
+    }
+    for (b = 0; b < num_lanes; ++b) {
+        int a = d, k = -1, last = -1;
+        double z = 0.0, target, cum = 0.0;
+        for (i = 0; i < d; ++i)
+            if ((drafts[b * d + i] < 0 || drafts[b * d + i] >= vocab) && status)
+                *status |= ST_BAD_DRAFT;
+        for (i = 0; i < d; ++i) {
+            const int xi = drafts[b * d + i];
+            if (xi < 0 || xi >= vocab) {
+                a = i;
+                break;
+            }
+            softmax_row(logits + ((size_t)b * window + i) * vocab, vocab, p);
+            if (!((double)u_accept[b * d + i] * (double)draft_probs[((size_t)b * d + i) * vocab + xi] < p[xi])) {
+                a = i;
+                break;
+            }
+        }
+        softmax_row(logits + ((size_t)b * window + a) * vocab, vocab, p);
+        for (x = 0; x < vocab; ++x) {
+            w[x] = p[x];
+            if (a < d) {
+                const double r = p[x] - (double)draft_probs[((size_t)b * d + a) * vocab + x];
+                w[x] = r > 0.0 ? r : 0.0;
+            }
+            z += w[x];
+        }
+        if (!(z > 0.0)) {
+            z = 0.0;
+            for (x = 0; x < vocab; ++x) {
+                w[x] = p[x];
+                z += w[x];
+            }
+        }
+        target = (double)u_sample[b] * z;
+        for (x = 0; x < vocab; ++x) {
+            if (w[x] > 0.0)
+                last = x;
+            cum += w[x];
+            if (k < 0 && cum > target)
+                k = x;
+        }
+        if (k < 0)
+            k = last;
+        for (i = 0; i < window; ++i)
+            out_tokens[b * window + i] = i < a ? drafts[b * d + i] : (i == a ? k : -1);
+        accept_len[b] = a;
+        if (seq_lens_inout)
+            seq_lens_inout[b] += 1 + a;
+    }
+    free(p);
+    free(w);
     return 0;
 }
