@@ -17,6 +17,8 @@ One JSON line (rank 0):
   spec_accept_lazy  the acceptance that reads each lane's logits rows only up
                to its first disagreement (timed apart, after the main loop),
                with the step rate it would give
+  spec_accept_sampled  lossless stochastic acceptance with a synthetic draft
+               distribution (timed apart likewise)
   clocks       nvidia-smi SM clocks and throttle reasons during the timed steps
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an untimed L2
@@ -389,6 +391,45 @@ def run_gpu(args):
                 "eager_us": float(np.mean(t_acc)) * 1e3, "step_us": lazy_step_us, "steps_per_s": 1e6 / lazy_step_us,
                 "timing": "CUDA events around the call after an L2 flush, same steps and warm-up as the main loop"}
 
+    # ---- lossless stochastic acceptance with the draft distribution q ----
+    sampled = None
+    if logits is not None:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(spec.seed)
+        # a draft distribution correlated with the target, drafts drawn from it
+        zq = 0.8 * logits[:, :W - 1] + 0.6 * torch.randn(logits[:, :W - 1].shape, generator=gen, device=dev)
+        qd = torch.softmax(zq, dim=2).contiguous()
+        del zq
+        dq = torch.multinomial(qd.view(-1, spec.vocab), 1, generator=gen).view(B, W - 1).to(torch.int32).contiguous()
+        ua = torch.rand((B, W - 1), generator=gen, device=dev)
+        us = torch.rand(B, generator=gen, device=dev)
+        ws = torch.empty(sdva.spec_accept_sampled_workspace_size(B, W), dtype=torch.uint8, device=dev)
+        s_acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        s_tok = torch.zeros((B, W), dtype=torch.int32, device=dev)
+        s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for k in range(args.warmup + args.steps):
+            flush_l2()
+            if k >= args.warmup:
+                s_ev[k - args.warmup][0].record(stream)
+            sdva.spec_accept_sampled(logits, qd, dq, ua, us, s_acc, s_tok, ws, commit_lens, vs.status)
+            if k >= args.warmup:
+                s_ev[k - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
+        t_s = float(np.mean([e[0].elapsed_time(e[1]) for e in s_ev]))
+        a_s = s_acc.cpu().numpy()
+        # every logits row for the statistics, then per lane the drawn row and,
+        # after a rejection, its draft row; one logit and one q entry per tested draft
+        s_bytes = (B * W * spec.vocab * 4 + B * spec.vocab * 4 + int((a_s < W - 1).sum()) * spec.vocab * 4
+                   + int(np.minimum(a_s + 1, W - 1).sum()) * 16)
+        s_step_us = (float(np.mean(t_app)) + float(np.mean(t_att)) + t_s) * 1e3
+        sampled = {"us": t_s * 1e3, "accept_len": [int(a) for a in a_s], "bytes_read": s_bytes,
+                   "gbs": s_bytes / (t_s / 1e3) / 1e9, "step_us": s_step_us, "steps_per_s": 1e6 / s_step_us,
+                   "inputs": "q = softmax(0.8 * target logits + 0.6 * N(0,1)), drafts drawn from q, uniforms "
+                             "from a seeded device generator",
+                   "timing": "CUDA events around the call after an L2 flush, same steps and warm-up as the main loop"}
+        del qd
+
     # ---- e2e: host buffers through the public API ----
     host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("kw", kw), ("vw", vw))}
     if logits is not None:
@@ -469,6 +510,7 @@ def run_gpu(args):
                      "traffic": traffic, "algorithmic_bytes": alg},
         "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "spec_accept_lazy": lazy,
+        "spec_accept_sampled": sampled,
         "gpu_launches": args.steps * (1 + 2 + (2 if logits is not None else 0)),
         "clocks": clocks,
         "wall_s_timed_loop": wall,

@@ -21,6 +21,8 @@
  *                       prefix, optional commit of the new lengths
  *   spec_accept_lazy -- the same acceptance reading each lane's rows only up
  *                       to its first disagreement, with per-lane draft counts
+ *   spec_accept_sampled -- lossless stochastic acceptance with the draft
+ *                       distribution (ratio test, residual draw)
  *
  * Conventions for every call
  *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA
@@ -266,6 +268,42 @@ int spec_accept(const float* logits, int num_lanes, int window, int vocab, const
 int spec_accept_lazy(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
                      const int32_t* num_drafts, int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout,
                      int32_t* status, sdva_stream_t stream);
+
+/*
+ * spec_accept_sampled -- lossless stochastic acceptance of a verify window
+ * (sampling at temperature 1 that keeps the target model's distribution).
+ *   DFlash2 keeps the draft model's conditional distribution q (NInfer
+ *   review, section "아키텍처 ③"); with it, the verifier accepts draft i when
+ *   u_i * q_i(x_i) < p_i(x_i), p_i = softmax(logits row i); at the first
+ *   rejection a it draws one token from max(0, p_a - q_a) normalised, and
+ *   from p_d when all d = window - 1 drafts are accepted.  The draw is the
+ *   inverse CDF in index order at u_sample * Z (Z = the weights' sum): the
+ *   smallest k whose running sum exceeds it, else the last index of positive
+ *   weight; a residual of zero mass falls back to p_a.
+ *   logits     : fp32 [num_lanes][window][vocab], finite.
+ *   draft_probs: fp32 [num_lanes][window - 1][vocab]: row i is q_i, the
+ *                distribution drafts[b][i] was drawn from (non-negative;
+ *                need not be renormalised).  Nullable when window == 1.
+ *   drafts     : int32 [num_lanes][window - 1] (nullable when window == 1).
+ *   u_accept   : fp32 [num_lanes][window - 1] uniforms in [0, 1).
+ *   u_sample   : fp32 [num_lanes] uniforms in [0, 1).
+ *   accept_len : int32 [num_lanes] (out): a.
+ *   out_tokens : int32 [num_lanes][window] (out): drafts[b][0 .. a), the
+ *                drawn token at position a, -1 after.
+ *   seq_lens_inout: nullable int32 [num_lanes] (in/out): adds 1 + a.
+ *   workspace  : device memory of spec_accept_sampled_workspace_size()
+ *                bytes, 8-byte aligned (per-row softmax statistics).
+ * Arithmetic is fp32 (hardware exp2): a decision within fp32 rounding of its
+ * boundary may differ from an exact evaluation.  An out-of-vocabulary draft
+ * is a rejection and sets SDVA_STATUS_BAD_DRAFT.  window 1 .. 16,
+ * num_lanes * window <= 65535.  Returns SDVA_OK, SDVA_ERR_INVALID,
+ * SDVA_ERR_UNSUPPORTED, SDVA_ERR_WORKSPACE or SDVA_ERR_CUDA.
+ */
+size_t spec_accept_sampled_workspace_size(int num_lanes, int window);
+int spec_accept_sampled(const float* logits, const float* draft_probs, int num_lanes, int window, int vocab,
+                        const int32_t* drafts, const float* u_accept, const float* u_sample, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* seq_lens_inout, void* workspace, size_t workspace_bytes,
+                        int32_t* status, sdva_stream_t stream);
 
 /* Static description of a return code or status bit set (never NULL). */
 const char* sdva_status_string(int code);

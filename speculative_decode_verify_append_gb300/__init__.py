@@ -14,6 +14,9 @@ The calls mirror ``include/sdva.h``:
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
     spec_accept_lazy(logits, drafts, accept_len, out_tokens, num_drafts=None, seq_lens_inout=None, status=None,
                      stream=None)
+    spec_accept_sampled_workspace_size(num_lanes, window)
+    spec_accept_sampled(logits, draft_probs, drafts, u_accept, u_sample, accept_len, out_tokens, workspace,
+                        seq_lens_inout=None, status=None, stream=None)
     sdva_status_string(code)
 """
 from __future__ import annotations
@@ -84,11 +87,15 @@ _lib.spec_accept.restype = _I
 _lib.spec_accept.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
 _lib.spec_accept_lazy.restype = _I
 _lib.spec_accept_lazy.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+_lib.spec_accept_sampled_workspace_size.restype = ctypes.c_size_t
+_lib.spec_accept_sampled_workspace_size.argtypes = [_I, _I]
+_lib.spec_accept_sampled.restype = _I
+_lib.spec_accept_sampled.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
-            "spec_accept_lazy", "sdva_status_string")
+            "spec_accept_lazy", "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -260,6 +267,31 @@ def spec_accept_lazy(logits: torch.Tensor, drafts: torch.Tensor | None, accept_l
                                _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"),
                                _dptr(status, torch.int32, "status"), _stream(stream))
     _check("spec_accept_lazy", rc)
+
+
+def spec_accept_sampled_workspace_size(num_lanes: int, window: int) -> int:
+    return int(_lib.spec_accept_sampled_workspace_size(num_lanes, window))
+
+
+def spec_accept_sampled(logits: torch.Tensor, draft_probs: torch.Tensor | None, drafts: torch.Tensor | None,
+                        u_accept: torch.Tensor | None, u_sample: torch.Tensor, accept_len: torch.Tensor,
+                        out_tokens: torch.Tensor, workspace: torch.Tensor, seq_lens_inout: torch.Tensor | None = None,
+                        status: torch.Tensor | None = None, stream=None) -> None:
+    """logits fp32 [B][W][V]; draft_probs fp32 [B][W-1][V]; drafts int32 [B][W-1];
+    u_accept fp32 [B][W-1]; u_sample fp32 [B]; workspace: uint8 device tensor of at
+    least spec_accept_sampled_workspace_size(B, W) bytes."""
+    B, W, V = logits.shape
+    rc = _lib.spec_accept_sampled(_dptr(logits, torch.float32, "logits"),
+                                  _dptr(draft_probs, torch.float32, "draft_probs") if W > 1 else None, B, W, V,
+                                  _dptr(drafts, torch.int32, "drafts") if W > 1 else None,
+                                  _dptr(u_accept, torch.float32, "u_accept") if W > 1 else None,
+                                  _dptr(u_sample, torch.float32, "u_sample"),
+                                  _dptr(accept_len, torch.int32, "accept_len"),
+                                  _dptr(out_tokens, torch.int32, "out_tokens"),
+                                  _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"),
+                                  _dptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                                  _dptr(status, torch.int32, "status"), _stream(stream))
+    _check("spec_accept_sampled", rc)
 
 
 def raw_library() -> ctypes.CDLL:

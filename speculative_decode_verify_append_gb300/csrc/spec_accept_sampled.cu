@@ -1,0 +1,365 @@
+// spec_accept_sampled.cu -- lossless stochastic acceptance of a verify window.
+//
+// DFlash2 keeps the draft model's real conditional distribution q (NInfer
+// review, section "아키텍처 ③"), which is what an acceptance that preserves
+// the target distribution needs: with p_i = softmax(logits row i), draft i
+// is accepted when u_i * q_i(x_i) < p_i(x_i); at the first rejection a, one
+// token is drawn from max(0, p_a - q_a) (normalised), and from p_d when every
+// draft is accepted.  The uniforms are inputs; the draw is the inverse CDF in
+// index order at u_sample * Z: the smallest k whose running sum exceeds it,
+// else the last k of positive weight; a residual of zero mass falls back to
+// p_a.
+//
+// Kernel 1 (row statistics): one cluster of up to 8 CTAs per logits row; each
+// CTA reduces its slice to (running max, sum of exp) with 16-byte streaming
+// loads, the cluster combines the slices in rank order through distributed
+// shared memory, and rank 0 stores (M, S) of the row in the workspace.  All
+// rows are reduced at once over the whole GPU (the acceptance needs S of
+// every row up to the first rejection).
+// Kernel 2 (accept and draw, programmatic dependent of kernel 1): one cluster
+// per lane.  Every CTA evaluates the ratio tests of the lane's drafts
+// identically, so all agree on a.  The CTAs then split row a: each walks its
+// slice in tiles of 4 x 256 consecutive logits, a block scan giving the
+// running sum of the weights in index order, and sends its slice total to
+// every CTA of the cluster; the CTA whose running range holds the target
+// walks its slice again with the same arithmetic and stops inside the tile
+// and the 4-logit group where the running sum crosses it.
+#include <cooperative_groups.h>
+
+#include "sdva_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sdva {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxCluster = 8;
+constexpr int kTile = 4 * kThreads;  // logits per tile of the walk
+constexpr int kSampleSlice = 4096;   // minimum logits per CTA of a lane's cluster
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Stat {
+  float m, s;  // running max, sum of exp(x - m)
+};
+
+__device__ __forceinline__ Stat combine(Stat a, Stat b) {
+  if (a.s == 0.0f) return b;
+  if (b.s == 0.0f) return a;
+  const float m = fmaxf(a.m, b.m);
+  return {m, a.s * fast_exp2((a.m - m) * kLog2e) + b.s * fast_exp2((b.m - m) * kLog2e)};
+}
+
+__device__ __forceinline__ Stat add4(Stat st, float4 v) {
+  const float m4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  const float m = st.s == 0.0f ? m4 : fmaxf(st.m, m4);
+  float s = st.s == 0.0f ? 0.0f : st.s * fast_exp2((st.m - m) * kLog2e);
+  s += fast_exp2((v.x - m) * kLog2e) + fast_exp2((v.y - m) * kLog2e) + fast_exp2((v.z - m) * kLog2e) +
+       fast_exp2((v.w - m) * kLog2e);
+  return {m, s};
+}
+
+// four consecutive values starting at index i of x (i % 4 == 0 when kVec);
+// entries at or past `end` read as `fill`
+template <bool kVec>
+__device__ __forceinline__ float4 load4(const float* x, int i, int end, float fill) {
+  if (kVec && i + 3 < end) return __ldcs(reinterpret_cast<const float4*>(x + i));
+  return make_float4(i < end ? x[i] : fill, i + 1 < end ? x[i + 1] : fill, i + 2 < end ? x[i + 2] : fill,
+                     i + 3 < end ? x[i + 3] : fill);
+}
+
+// grid (parts, rows), cluster (parts, 1, 1); stats[row] = (M, S)
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* logits, int vocab, int chunk,
+                                                            float2* stats) {
+  cg::cluster_group cluster = cg::this_cluster();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ Stat s_w[kThreads / 32];
+  __shared__ Stat c_st[kMaxCluster];  // in rank 0: one entry per CTA of the cluster
+  const int part = blockIdx.x, row = blockIdx.y;
+  const float* x = logits + (size_t)row * vocab;
+  const int lo = part * chunk, hi = min(vocab, lo + chunk);
+  Stat st = {0.0f, 0.0f};
+  const float ninf = __int_as_float(0xff800000);
+  for (int i = lo + 4 * (int)threadIdx.x; i < hi; i += 4 * kThreads) {
+    const float4 v = load4<kVec>(x, i, hi, ninf);
+    st = add4(st, v);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const Stat o = {__shfl_xor_sync(0xffffffffu, st.m, off), __shfl_xor_sync(0xffffffffu, st.s, off)};
+    st = combine(st, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_w[warp] = st;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) st = combine(st, s_w[w]);
+    *cluster.map_shared_rank(&c_st[part], 0) = st;
+  }
+  cluster.sync();
+  if (part == 0 && threadIdx.x == 0) {
+    Stat t = c_st[0];
+    for (int p = 1; p < (int)gridDim.x; ++p) t = combine(t, c_st[p]);
+    stats[row] = make_float2(t.m, t.s);
+  }
+  cluster.sync();  // rank 0's shared memory must outlive the other CTAs' stores
+}
+
+// Scan of v over the block in thread order: *incl and *excl are this
+// thread's inclusive and exclusive sums, the return value the block's sum.
+// Each thread's exclusive sum is bitwise its predecessor's inclusive sum and
+// the block's sum is bitwise the last thread's inclusive sum, so the ranges
+// (excl, incl] tile (0, total] without gaps.
+__device__ __forceinline__ float block_scan(float v, float* s_part, float* incl, float* excl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  const float prev = __shfl_up_sync(0xffffffffu, v, 1);
+  if (lane == 31) s_part[warp] = v;
+  __syncthreads();
+  float before = 0.0f, all = 0.0f;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) before += s_part[w];
+    all += s_part[w];
+  }
+  __syncthreads();  // s_part is reused by the next call
+  *incl = before + v;
+  *excl = lane > 0 ? before + prev : before;
+  return all;
+}
+
+struct Row {
+  const float* l;   // logits row
+  const float* q;   // draft row (residual) or nullptr (draw from p)
+  float m, inv_s;   // p(x) = exp(l[x] - m) * inv_s
+};
+
+__device__ __forceinline__ float weight(const Row& r, float lx, float qx) {
+  const float p = fast_exp2((lx - r.m) * kLog2e) * r.inv_s;
+  if (r.q == nullptr) return p;
+  const float w = p - qx;
+  return w > 0.0f ? w : 0.0f;
+}
+
+// Walk [lo, hi) in tiles of kTile logits, keeping the running sum of the
+// weights in index order.  search == false: returns the slice's total.
+// search == true: stops in the tile, the thread and the logit where the
+// running sum first exceeds `target` and stores that index in *found; when
+// it never does (the target sits within rounding of the slice's end), the
+// last index of positive weight.  Both modes do the same arithmetic, so a
+// target below the first mode's total is always crossed.
+template <bool kVec>
+__device__ float walk(const Row& r, int lo, int hi, bool search, float target, float* s_part, int* s_found,
+                      int* found) {
+  float running = 0.0f;
+  int last_pos = -1;
+  const float ninf = __int_as_float(0xff800000);
+  for (int base = lo; base < hi; base += kTile) {
+    const int i = base + 4 * (int)threadIdx.x;
+    const float4 l4 = load4<kVec>(r.l, i, hi, ninf);
+    const float4 q4 = r.q != nullptr ? load4<kVec>(r.q, i, hi, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float w[4] = {weight(r, l4.x, q4.x), weight(r, l4.y, q4.y), weight(r, l4.z, q4.z),
+                        weight(r, l4.w, q4.w)};
+    const float ts = (w[0] + w[1]) + (w[2] + w[3]);
+    float incl, excl;
+    const float tile_total = block_scan(ts, s_part, &incl, &excl);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (w[j] > 0.0f) last_pos = i + j;
+    if (search && running + tile_total > target) {
+      // exactly one thread's range (running + excl, running + incl] holds the target
+      if (running + excl <= target && running + incl > target) {
+        float cum = excl;
+        int k = -1, lastj = -1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (w[j] > 0.0f) lastj = i + j;
+          cum += w[j];
+          if (k < 0 && running + cum > target) k = i + j;
+        }
+        *s_found = k >= 0 ? k : lastj;  // lastj: the 4-term sum rounded past the target
+      }
+      __syncthreads();
+      break;
+    }
+    running += tile_total;
+  }
+  if (search) {
+    if (*s_found < 0) atomicMax(s_found, last_pos);
+    __syncthreads();
+    *found = *s_found;
+  }
+  return running;
+}
+
+// grid (parts, lanes), cluster (parts, 1, 1)
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) accept_sample_kernel(
+    const float* logits, const float* draft_probs, int window, int vocab, int chunk, const int32_t* drafts,
+    const float* u_accept, const float* u_sample, const float2* stats, int32_t* accept_len, int32_t* out_tokens,
+    int32_t* seq_lens, int32_t* status) {
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float s_part[kThreads / 32];
+  __shared__ float c_tot[2][kMaxCluster];  // slice totals of the two possible passes
+  __shared__ int s_rej;
+  __shared__ int s_found;
+  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
+  const int d = window - 1;
+  if (threadIdx.x == 0) {
+    s_rej = d;
+    s_found = -1;
+  }
+  // kernel 1's statistics are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  if ((int)threadIdx.x < d) {
+    const int i = threadIdx.x, x = drafts[(size_t)b * d + i];
+    bool accept = false;
+    if (x < 0 || x >= vocab) {
+      if (part == 0) raise_status(status, SDVA_STATUS_BAD_DRAFT);
+    } else {
+      const float2 st = stats[(size_t)b * window + i];
+      const float lx = logits[((size_t)b * window + i) * vocab + x];
+      const float px = fast_exp2((lx - st.x) * kLog2e) / st.y;
+      const float qx = draft_probs[((size_t)b * d + i) * vocab + x];
+      accept = u_accept[(size_t)b * d + i] * qx < px;
+    }
+    if (!accept) atomicMin(&s_rej, i);
+  }
+  __syncthreads();
+  const int a = s_rej;
+  const float2 st = stats[(size_t)b * window + a];
+  Row r;
+  r.l = logits + ((size_t)b * window + a) * vocab;
+  r.q = a < d ? draft_probs + ((size_t)b * d + a) * vocab : nullptr;
+  r.m = st.x;
+  r.inv_s = 1.0f / st.y;
+  const int lo = part * chunk, hi = min(vocab, lo + chunk);
+  float z = 0.0f;
+  int pass = 0;
+  for (;; ++pass) {
+    const float total = walk<kVec>(r, lo, hi, false, 0.0f, s_part, &s_found, nullptr);
+    if (threadIdx.x < (unsigned)parts) *cluster.map_shared_rank(&c_tot[pass][part], threadIdx.x) = total;
+    cluster.sync();
+    z = 0.0f;
+    for (int p = 0; p < parts; ++p) z += c_tot[pass][p];
+    // a residual of zero mass falls back to p_a (the same decision in every CTA)
+    if (z > 0.0f || pass == 1 || r.q == nullptr) break;
+    r.q = nullptr;
+  }
+  // the CTA whose running range holds the target draws the token
+  const float target = u_sample[b] * z;
+  int owner = -1, last = -1;
+  float before = 0.0f, cum = 0.0f;
+  for (int p = 0; p < parts; ++p) {
+    const float t = c_tot[pass][p];
+    if (t > 0.0f) last = p;
+    if (owner < 0 && cum + t > target) {
+      owner = p;
+      before = cum;
+    }
+    cum += t;
+  }
+  // no crossing (the target sits within rounding of the row's end): the last
+  // CTA with weight takes its last index of positive weight
+  const bool crossing = owner >= 0;
+  if (!crossing) owner = last;
+  if (owner < 0) {
+    // no positive weight in the row (only non-finite logits give this)
+    if (part == 0 && threadIdx.x == 0) out_tokens[(size_t)b * window + a] = 0;
+  } else if (part == owner) {
+    int k = -1;
+    walk<kVec>(r, lo, hi, true, crossing ? target - before : __int_as_float(0x7f800000), s_part, &s_found, &k);
+    if (threadIdx.x == 0) out_tokens[(size_t)b * window + a] = k;
+  }
+  if (part == 0 && threadIdx.x == 0) {
+    int32_t* tok = out_tokens + (size_t)b * window;
+    for (int i = 0; i < window; ++i)
+      if (i != a) tok[i] = i < a ? drafts[(size_t)b * d + i] : -1;
+    accept_len[b] = a;
+    if (seq_lens != nullptr) seq_lens[b] += 1 + a;
+  }
+  // no exchange follows the last barrier, so CTAs may leave in any order
+}
+
+bool vectorizable(const float* p, int vocab) {
+  return (vocab & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace
+}  // namespace sdva
+
+using namespace sdva;
+
+extern "C" size_t spec_accept_sampled_workspace_size(int num_lanes, int window) {
+  if (num_lanes <= 0 || window <= 0) return 0;
+  return (((size_t)num_lanes * window * sizeof(float2)) + 255) & ~(size_t)255;
+}
+
+extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs, int num_lanes, int window,
+                                   int vocab, const int32_t* drafts, const float* u_accept, const float* u_sample,
+                                   int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout,
+                                   void* workspace, size_t workspace_bytes, int32_t* status, sdva_stream_t stream) {
+  if (logits == nullptr || u_sample == nullptr || accept_len == nullptr || out_tokens == nullptr)
+    return SDVA_ERR_INVALID;
+  if (num_lanes <= 0 || window <= 0 || vocab <= 0) return SDVA_ERR_INVALID;
+  if (window > 1 && (draft_probs == nullptr || drafts == nullptr || u_accept == nullptr)) return SDVA_ERR_INVALID;
+  if (window > kMaxWindow) return SDVA_ERR_UNSUPPORTED;
+  const long long rows = (long long)num_lanes * window;
+  if (rows > 65535) return SDVA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < spec_accept_sampled_workspace_size(num_lanes, window) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 7u))
+    return SDVA_ERR_WORKSPACE;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDVA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float2* stats = static_cast<float2*>(workspace);
+  const bool vec = vectorizable(logits, vocab) && (window == 1 || vectorizable(draft_probs, vocab));
+  {
+    // CTAs per row: enough to cover every SM about four times, at most one portable cluster
+    int parts = 1;
+    while (parts < kMaxCluster && rows * parts < 4LL * sms) parts *= 2;
+    const int chunk = (((vocab + parts - 1) / parts) + 3) & ~3;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(parts, (unsigned)rows, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = parts;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const auto kernel = vec ? row_stats_kernel<true> : row_stats_kernel<false>;
+    if (cudaLaunchKernelEx(&cfg, kernel, logits, vocab, chunk, stats) != cudaSuccess) return SDVA_ERR_CUDA;
+  }
+  {
+    const int parts = min(kMaxCluster, max(1, (vocab + kSampleSlice - 1) / kSampleSlice));
+    const int chunk = (((vocab + parts - 1) / parts) + 3) & ~3;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(parts, (unsigned)num_lanes, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = parts;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const auto kernel = vec ? accept_sample_kernel<true> : accept_sample_kernel<false>;
+    if (cudaLaunchKernelEx(&cfg, kernel, logits, draft_probs, window, vocab, chunk, drafts, u_accept, u_sample,
+                           (const float2*)stats, accept_len, out_tokens, seq_lens_inout, status) != cudaSuccess)
+      return SDVA_ERR_CUDA;
+  }
+  return SDVA_OK;
+}

@@ -123,6 +123,19 @@ def test_argument_validation_returns_before_cuda(lib):
     assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
     assert sa(fake, 0, 4, 100, fake, fake, fake, None, None, None) == -1
     assert sa(fake, 1, 17, 100, fake, fake, fake, None, None, None) == -2
+    ws = lib.spec_accept_sampled_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert ws(8, 16) >= 8 * 16 * 8 and ws(8, 16) % 256 == 0 and ws(0, 4) == 0
+    sm = lib.spec_accept_sampled
+    sm.restype = ctypes.c_int
+    sm.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    assert sm(fake, None, 2, 4, 100, fake, fake, fake, fake, fake, None, fake, 4096, None, None) == -1  # q needed
+    assert sm(fake, fake, 2, 4, 100, fake, fake, None, fake, fake, None, fake, 4096, None, None) == -1  # u_sample
+    assert sm(fake, fake, 2, 17, 100, fake, fake, fake, fake, fake, None, fake, 4096, None, None) == -2
+    assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, fake, 8, None, None) == -3  # too small
+    assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, None, 4096, None, None) == -3
+    assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, P(0x1004), 4096, None, None) == -3
     lz = lib.spec_accept_lazy
     lz.restype = ctypes.c_int
     assert lz(fake, 1, 4, 100, None, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
