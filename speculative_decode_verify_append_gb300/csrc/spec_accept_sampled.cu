@@ -16,14 +16,16 @@
 // shared memory, and rank 0 stores (M, S) of the row in the workspace.  All
 // rows are reduced at once over the whole GPU (the acceptance needs S of
 // every row up to the first rejection).
-// Kernel 2 (accept and draw, programmatic dependent of kernel 1): one cluster
-// per lane.  Every CTA evaluates the ratio tests of the lane's drafts
-// identically, so all agree on a.  The CTAs then split row a: each walks its
-// slice in tiles of 4 x 256 consecutive logits, a block scan giving the
-// running sum of the weights in index order, and sends its slice total to
-// every CTA of the cluster; the CTA whose running range holds the target
-// walks its slice again with the same arithmetic and stops inside the tile
-// and the 4-logit group where the running sum crosses it.
+// Kernels 2 and 3 (the draw, each a programmatic dependent of the one before):
+// up to 64 CTAs per lane.  Every CTA evaluates the ratio tests of the lane's
+// drafts identically, so all agree on a.  Kernel 2: each CTA walks its slice
+// of row a in tiles of 4 x 256 consecutive logits, a block scan giving the
+// running sum of the weights in index order, and stores the slice's total.
+// Kernel 3: every CTA adds the lane's totals in slice order; the CTA whose
+// running range holds the target walks its slice again with the same
+// arithmetic and stops inside the tile and the 4-logit group where the
+// running sum crosses it.  (One cluster of 8 CTAs per lane, the first
+// design, spent most of its time pulling a whole row through 8 SMs.)
 #include <cooperative_groups.h>
 
 #include "sdva_common.cuh"
@@ -36,7 +38,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxCluster = 8;
 constexpr int kTile = 4 * kThreads;  // logits per tile of the walk
-constexpr int kSampleSlice = 4096;   // minimum logits per CTA of a lane's cluster
+constexpr int kSampleSlice = 4096;   // minimum logits per CTA of the draw
+constexpr int kMaxSlices = 64;       // CTAs per lane of the draw
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Stat {
@@ -196,31 +199,19 @@ __device__ float walk(const Row& r, int lo, int hi, bool search, float target, f
   return running;
 }
 
-// grid (parts, lanes), cluster (parts, 1, 1)
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads) accept_sample_kernel(
-    const float* logits, const float* draft_probs, int window, int vocab, int chunk, const int32_t* drafts,
-    const float* u_accept, const float* u_sample, const float2* stats, int32_t* accept_len, int32_t* out_tokens,
-    int32_t* seq_lens, int32_t* status) {
-  cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float s_part[kThreads / 32];
-  __shared__ float c_tot[2][kMaxCluster];  // slice totals of the two possible passes
-  __shared__ int s_rej;
-  __shared__ int s_found;
-  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
+// The lane's accept length a: every CTA evaluates the ratio tests with the
+// same fp32 arithmetic, so all CTAs of all launches agree.
+__device__ int accept_count(const float* logits, const float* draft_probs, int window, int vocab, int b,
+                            const int32_t* drafts, const float* u_accept, const float2* stats, int32_t* status,
+                            bool report, int* s_rej) {
   const int d = window - 1;
-  if (threadIdx.x == 0) {
-    s_rej = d;
-    s_found = -1;
-  }
-  // kernel 1's statistics are visible after this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *s_rej = d;
   __syncthreads();
   if ((int)threadIdx.x < d) {
     const int i = threadIdx.x, x = drafts[(size_t)b * d + i];
     bool accept = false;
     if (x < 0 || x >= vocab) {
-      if (part == 0) raise_status(status, SDVA_STATUS_BAD_DRAFT);
+      if (report) raise_status(status, SDVA_STATUS_BAD_DRAFT);
     } else {
       const float2 st = stats[(size_t)b * window + i];
       const float lx = logits[((size_t)b * window + i) * vocab + x];
@@ -228,35 +219,91 @@ __global__ void __launch_bounds__(kThreads) accept_sample_kernel(
       const float qx = draft_probs[((size_t)b * d + i) * vocab + x];
       accept = u_accept[(size_t)b * d + i] * qx < px;
     }
-    if (!accept) atomicMin(&s_rej, i);
+    if (!accept) atomicMin(s_rej, i);
   }
   __syncthreads();
-  const int a = s_rej;
+  return *s_rej;
+}
+
+__device__ __forceinline__ Row draw_row(const float* logits, const float* draft_probs, int window, int vocab, int b,
+                                        int a, const float2* stats) {
+  const int d = window - 1;
   const float2 st = stats[(size_t)b * window + a];
   Row r;
   r.l = logits + ((size_t)b * window + a) * vocab;
   r.q = a < d ? draft_probs + ((size_t)b * d + a) * vocab : nullptr;
   r.m = st.x;
   r.inv_s = 1.0f / st.y;
-  const int lo = part * chunk, hi = min(vocab, lo + chunk);
-  float z = 0.0f;
-  int pass = 0;
-  for (;; ++pass) {
-    const float total = walk<kVec>(r, lo, hi, false, 0.0f, s_part, &s_found, nullptr);
-    if (threadIdx.x < (unsigned)parts) *cluster.map_shared_rank(&c_tot[pass][part], threadIdx.x) = total;
-    cluster.sync();
-    z = 0.0f;
-    for (int p = 0; p < parts; ++p) z += c_tot[pass][p];
-    // a residual of zero mass falls back to p_a (the same decision in every CTA)
-    if (z > 0.0f || pass == 1 || r.q == nullptr) break;
+  return r;
+}
+
+struct SampleArgs {
+  const float* logits;
+  const float* draft_probs;
+  const int32_t* drafts;
+  const float* u_accept;
+  const float* u_sample;
+  const float2* stats;  // [B][W]: (M, S) of every row
+  float2* totals;       // [B][kMaxSlices]: per slice, (residual weight, p weight) of the drawn row
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  int32_t* seq_lens;
+  int32_t* status;
+  int window, vocab, chunk;
+};
+
+// grid (slices, lanes); programmatic dependent of the statistics kernel.
+// Each CTA finds a and stores its slice's total weight of the drawn row (and
+// the total of p_a, for a residual of zero mass).
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) sample_totals_kernel(SampleArgs g) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float s_part[kThreads / 32];
+  __shared__ int s_rej;
+  const int part = blockIdx.x, b = blockIdx.y;
+  const int a = accept_count(g.logits, g.draft_probs, g.window, g.vocab, b, g.drafts, g.u_accept, g.stats,
+                             g.status, part == 0, &s_rej);
+  Row r = draw_row(g.logits, g.draft_probs, g.window, g.vocab, b, a, g.stats);
+  const int lo = part * g.chunk, hi = min(g.vocab, lo + g.chunk);
+  const float res = walk<kVec>(r, lo, hi, false, 0.0f, s_part, nullptr, nullptr);
+  float pt = res;
+  if (r.q != nullptr) {
     r.q = nullptr;
+    pt = walk<kVec>(r, lo, hi, false, 0.0f, s_part, nullptr, nullptr);
   }
-  // the CTA whose running range holds the target draws the token
-  const float target = u_sample[b] * z;
+  if (threadIdx.x == 0) g.totals[(size_t)b * kMaxSlices + part] = make_float2(res, pt);
+}
+
+// grid (slices, lanes); programmatic dependent of the totals kernel.  Every
+// CTA adds the lane's slice totals in slice order and finds the slice whose
+// running range holds u_sample * Z; that CTA walks its slice again (the same
+// arithmetic) to the crossing.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) sample_draw_kernel(SampleArgs g) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float s_part[kThreads / 32];
+  __shared__ float2 s_tot[kMaxSlices];
+  __shared__ int s_rej, s_found;
+  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
+  if (threadIdx.x == 0) s_found = -1;
+  if ((int)threadIdx.x < parts) s_tot[threadIdx.x] = g.totals[(size_t)b * kMaxSlices + threadIdx.x];
+  const int a = accept_count(g.logits, g.draft_probs, g.window, g.vocab, b, g.drafts, g.u_accept, g.stats,
+                             g.status, false, &s_rej);
+  Row r = draw_row(g.logits, g.draft_probs, g.window, g.vocab, b, a, g.stats);
+  float z = 0.0f;
+  for (int p = 0; p < parts; ++p) z += s_tot[p].x;
+  const bool use_p = !(z > 0.0f) && r.q != nullptr;  // a residual of zero mass falls back to p_a
+  if (use_p) {
+    r.q = nullptr;
+    z = 0.0f;
+    for (int p = 0; p < parts; ++p) z += s_tot[p].y;
+  }
+  const float target = g.u_sample[b] * z;
   int owner = -1, last = -1;
   float before = 0.0f, cum = 0.0f;
   for (int p = 0; p < parts; ++p) {
-    const float t = c_tot[pass][p];
+    const float t = use_p ? s_tot[p].y : s_tot[p].x;
     if (t > 0.0f) last = p;
     if (owner < 0 && cum + t > target) {
       owner = p;
@@ -265,25 +312,26 @@ __global__ void __launch_bounds__(kThreads) accept_sample_kernel(
     cum += t;
   }
   // no crossing (the target sits within rounding of the row's end): the last
-  // CTA with weight takes its last index of positive weight
+  // slice with weight takes its last index of positive weight
   const bool crossing = owner >= 0;
   if (!crossing) owner = last;
+  int32_t* tok = g.out_tokens + (size_t)b * g.window;
   if (owner < 0) {
     // no positive weight in the row (only non-finite logits give this)
-    if (part == 0 && threadIdx.x == 0) out_tokens[(size_t)b * window + a] = 0;
+    if (part == 0 && threadIdx.x == 0) tok[a] = 0;
   } else if (part == owner) {
+    const int lo = part * g.chunk, hi = min(g.vocab, lo + g.chunk);
     int k = -1;
     walk<kVec>(r, lo, hi, true, crossing ? target - before : __int_as_float(0x7f800000), s_part, &s_found, &k);
-    if (threadIdx.x == 0) out_tokens[(size_t)b * window + a] = k;
+    if (threadIdx.x == 0) tok[a] = k;
   }
   if (part == 0 && threadIdx.x == 0) {
-    int32_t* tok = out_tokens + (size_t)b * window;
-    for (int i = 0; i < window; ++i)
-      if (i != a) tok[i] = i < a ? drafts[(size_t)b * d + i] : -1;
-    accept_len[b] = a;
-    if (seq_lens != nullptr) seq_lens[b] += 1 + a;
+    const int d = g.window - 1;
+    for (int i = 0; i < g.window; ++i)
+      if (i != a) tok[i] = i < a ? g.drafts[(size_t)b * d + i] : -1;
+    g.accept_len[b] = a;
+    if (g.seq_lens != nullptr) g.seq_lens[b] += 1 + a;
   }
-  // no exchange follows the last barrier, so CTAs may leave in any order
 }
 
 bool vectorizable(const float* p, int vocab) {
@@ -295,9 +343,15 @@ bool vectorizable(const float* p, int vocab) {
 
 using namespace sdva;
 
+namespace {
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+}  // namespace
+
+// per-row statistics [B][W], then per-slice totals of the drawn rows [B][kMaxSlices]
 extern "C" size_t spec_accept_sampled_workspace_size(int num_lanes, int window) {
   if (num_lanes <= 0 || window <= 0) return 0;
-  return (((size_t)num_lanes * window * sizeof(float2)) + 255) & ~(size_t)255;
+  return align256((size_t)num_lanes * window * sizeof(float2)) +
+         align256((size_t)num_lanes * kMaxSlices * sizeof(float2));
 }
 
 extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs, int num_lanes, int window,
@@ -340,26 +394,36 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
     const auto kernel = vec ? row_stats_kernel<true> : row_stats_kernel<false>;
     if (cudaLaunchKernelEx(&cfg, kernel, logits, vocab, chunk, stats) != cudaSuccess) return SDVA_ERR_CUDA;
   }
-  {
-    const int parts = min(kMaxCluster, max(1, (vocab + kSampleSlice - 1) / kSampleSlice));
-    const int chunk = (((vocab + parts - 1) / parts) + 3) & ~3;
+  SampleArgs g;
+  g.logits = logits;
+  g.draft_probs = draft_probs;
+  g.drafts = drafts;
+  g.u_accept = u_accept;
+  g.u_sample = u_sample;
+  g.stats = stats;
+  g.totals = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                       align256((size_t)num_lanes * window * sizeof(float2)));
+  g.accept_len = accept_len;
+  g.out_tokens = out_tokens;
+  g.seq_lens = seq_lens_inout;
+  g.status = status;
+  g.window = window;
+  g.vocab = vocab;
+  const int slices = min(kMaxSlices, max(1, (vocab + kSampleSlice - 1) / kSampleSlice));
+  g.chunk = (((vocab + slices - 1) / slices) + 3) & ~3;
+  for (int k = 0; k < 2; ++k) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(parts, (unsigned)num_lanes, 1);
+    cfg.gridDim = dim3(slices, (unsigned)num_lanes, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = parts;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    const auto kernel = vec ? accept_sample_kernel<true> : accept_sample_kernel<false>;
-    if (cudaLaunchKernelEx(&cfg, kernel, logits, draft_probs, window, vocab, chunk, drafts, u_accept, u_sample,
-                           (const float2*)stats, accept_len, out_tokens, seq_lens_inout, status) != cudaSuccess)
-      return SDVA_ERR_CUDA;
+    cfg.numAttrs = 1;
+    const auto kernel = k == 0 ? (vec ? sample_totals_kernel<true> : sample_totals_kernel<false>)
+                               : (vec ? sample_draw_kernel<true> : sample_draw_kernel<false>);
+    if (cudaLaunchKernelEx(&cfg, kernel, g) != cudaSuccess) return SDVA_ERR_CUDA;
   }
   return SDVA_OK;
 }
