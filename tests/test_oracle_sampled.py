@@ -133,3 +133,25 @@ def test_bonus_token_is_distributed_as_the_last_row():
     assert (acc == 1).all()
     ok, chi2, bound = _chi2_ok(np.bincount(tok[:, 1], minlength=V), p[1], N)
     assert ok, (chi2, bound)
+
+
+def test_zero_residual_falls_back_to_the_target():
+    # q = 3 p (not normalised): every draft is rejected at u = 0.5 and max(0, p - q)
+    # has no mass, so the token is drawn from p itself
+    rng = np.random.default_rng(55)
+    B, W, V = 6, 3, 25
+    logits = rng.standard_normal((B, W, V)).astype(np.float32)
+    p = np.exp(logits.astype(np.float64) - logits.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    q = (3.0 * p[:, :W - 1]).astype(np.float32)
+    drafts = rng.integers(0, V, size=(B, W - 1)).astype(np.int32)
+    ua = np.full((B, W - 1), 0.5, np.float32)
+    us = rng.random(B).astype(np.float32)
+    acc, tok, _, _ = oracle.spec_accept_sampled(logits, q, drafts, ua, us)
+    assert (acc == 0).all()
+    for b in range(B):
+        a, t = brute.accept_sampled(logits[b].astype(np.float64).tolist(), q[b].astype(np.float64).tolist(),
+                                    [int(x) for x in drafts[b]], [0.5] * (W - 1), float(us[b]))
+        assert (a, t) == (0, list(tok[b]))
+        cdf = np.cumsum(p[b, 0])
+        assert tok[b, 0] == int(np.searchsorted(cdf, us[b] * cdf[-1], side="right"))
