@@ -66,6 +66,10 @@ def _load():
             lib.oracle_verify_attn.restype = I
             lib.oracle_verify_attn.argtypes = [I, I, I, P, P, P, P, P, I, I, I, P, I, P, ctypes.c_float,
                                                P, P, I, I, P]
+            lib.oracle_tree_attn.restype = I
+            lib.oracle_tree_attn.argtypes = [I, I, I, P, P, P, P, P, I, I, I, P, I, P, P, ctypes.c_float, P, I, P]
+            lib.oracle_tree_accept.restype = I
+            lib.oracle_tree_accept.argtypes = [P, I, I, I, P, P, P, P, P, P, P]
             lib.oracle_decode_row.restype = I
             lib.oracle_decode_row.argtypes = [I, I, I, P, P, P, P, P, I, P, I, ctypes.c_float, P]
             lib.oracle_argmax.restype = I
@@ -215,6 +219,44 @@ def verify_attn(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_le
     if rc != 0:
         raise ValueError("oracle_verify_attn: invalid arguments")
     return out, int(st[0])
+
+
+def tree_attn(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
+              parent: np.ndarray, sm_scale: float, threads: int = 1) -> tuple[np.ndarray, int]:
+    """fp64 attention of a draft tree's window: row i sees the context and the
+    window keys of its ancestors and itself.  parent int32 [B][W] (entry 0
+    unused, 0 <= parent[i] < i).  Returns (out fp64 [B][W][Hq][128], status)."""
+    q = _as(q_bf16, np.uint16)
+    pt = _as(page_table, np.int32)
+    sl = _as(seq_lens, np.int32)
+    par = _as(parent, np.int32)
+    B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+    st = np.zeros(1, np.int32)
+    out = np.zeros((B, W, Hq, HEAD_DIM), np.float64)
+    rc = _load().oracle_tree_attn(*cache._args(), _ptr(q), Hq, B, W, _ptr(pt), pt.shape[1], _ptr(sl), _ptr(par),
+                                  float(sm_scale), _ptr(out), int(threads), _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle_tree_attn: invalid arguments")
+    return out, int(st[0])
+
+
+def tree_accept(logits: np.ndarray, tokens: np.ndarray, parent: np.ndarray, seq_lens: np.ndarray | None = None):
+    """Greedy acceptance of a draft tree.  logits [B][W][V]; tokens, parent int32
+    [B][W].  Returns (accept_len [B], path [B][W] of accepted slots (root first,
+    -1 after), out_tokens [B][W] (accepted tokens, the bonus, -1 after),
+    new seq_lens or None, status)."""
+    lg = _as(logits, np.float32)
+    B, W, V = lg.shape
+    tk = _as(tokens, np.int32).reshape(B, W)
+    par = _as(parent, np.int32).reshape(B, W)
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, W), np.int32)
+    tok = np.zeros((B, W), np.int32)
+    sl = None if seq_lens is None else _as(seq_lens, np.int32).copy()
+    st = np.zeros(1, np.int32)
+    _load().oracle_tree_accept(_ptr(lg), B, W, V, _ptr(tk), _ptr(par), _ptr(acc), _ptr(path), _ptr(tok), _ptr(sl),
+                               _ptr(st))
+    return acc, path, tok, sl, int(st[0])
 
 
 def decode_row(cache: Cache, q_row_bf16: np.ndarray, kv_head: int, page_row: np.ndarray, n_keys: int,

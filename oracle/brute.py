@@ -226,3 +226,46 @@ def accept_sampled(logits_rows, q_rows, drafts, u_accept, u_sample):
     if k is None:
         k = max(x for x in range(n) if w[x] > 0.0)
     return a, list(drafts[:a]) + [k] + [-1] * (len(logits_rows) - a - 1)
+
+
+def attention_keys(cache: Cache, q_bits, page_row, hk: int, positions, sm_scale: float):
+    """Attention of one query row over an explicit list of cached positions."""
+    import math
+    q = [bf16(b) for b in q_bits]
+    logits = []
+    for pos in positions:
+        pid, off = page_row[pos // PAGE], pos % PAGE
+        logits.append(sm_scale * math.fsum(q[d] * cache.value(0, pid, hk, off, d) for d in range(HEAD_DIM)))
+    m = max(logits)
+    w = [math.exp(x - m) for x in logits]
+    z = math.fsum(w)
+    out = []
+    for d in range(HEAD_DIM):
+        out.append(math.fsum(w[k] * cache.value(1, page_row[pos // PAGE], hk, pos % PAGE, d)
+                             for k, pos in enumerate(positions)) / z)
+    return out
+
+
+def tree_accept(logits_rows, tokens, parent):
+    """Draft-tree acceptance stated over root-to-node paths: a node is accepted
+    when every node on its path from the root carries the argmax of its
+    parent's row; among accepted nodes the deepest wins, ties to the path
+    that is smaller slot by slot.  Returns (a, path, out_tokens)."""
+    W = len(tokens)
+    t = [argmax(r) for r in logits_rows]
+
+    def chain(i):
+        out = [i]
+        while out[-1] != 0:
+            out.append(parent[out[-1]])
+        return out[::-1]
+
+    best = [0]
+    for i in range(1, W):
+        p = chain(i)
+        if all(tokens[p[k + 1]] == t[p[k]] for k in range(len(p) - 1)):
+            if len(p) > len(best) or (len(p) == len(best) and p < best):
+                best = p
+    a = len(best) - 1
+    out = [tokens[s] for s in best[1:]] + [t[best[-1]]]
+    return a, best + [-1] * (W - len(best)), out + [-1] * (W - len(out))

@@ -47,6 +47,14 @@
  *      drafts only drafts[b][0 .. d_b) are compared, and the rows after the
  *      first disagreement decide nothing, so the lazy form reports argmaxes
  *      only for rows 0 .. a and -1 after them.
+ *   R9 Draft trees (a reading: the pages describe chains of drafts only):
+ *      window slot 0 is the root (the last committed token) and slot i >= 1
+ *      has a parent slot parent[i] < i; the window is appended in slot order
+ *      as usual.  Row i attends to the context and to the window keys of its
+ *      ancestors and itself.  Acceptance walks from the root: at node n it
+ *      moves to the first child (in slot order) whose token is the argmax of
+ *      row n; a = the nodes accepted, the bonus token = the argmax of the
+ *      last node's row.
  *   R8 Lossless stochastic acceptance (DFlash2 keeps the draft model's
  *      conditional distribution q: NInfer review, section "아키텍처 ③"):
  *      p_i = softmax(logits row i) (temperature 1); draft i is accepted when
@@ -68,6 +76,7 @@
 
 #define PAGE 64
 #define HEAD_DIM 128
+#define MAX_WINDOW 16
 
 enum { ST_BAD_PAGE = 1, ST_OVERFLOW = 2, ST_BAD_DRAFT = 4, ST_BAD_COUNT = 16 };
 enum { KV_FP8 = 0, KV_INT4 = 1 };
@@ -390,6 +399,7 @@ typedef struct {
     double* out;
     const int32_t* rows; /* optional list of (b, i, h) triples */
     int nrows;
+    const int32_t* parent; /* optional [B][W] draft tree (R9); NULL: causal window */
     int next; /* work counter */
     pthread_mutex_t lock;
     int32_t status;
@@ -404,7 +414,7 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
     const int32_t* row = J->page_table + (size_t)b * J->max_pages;
     int L = J->seq_lens[b];
     int err = lane_check(c, row, J->max_pages, L, L + J->window);
-    int n, j, d;
+    int n, j, d, seen[MAX_WINDOW];
     const uint16_t* qrow;
     double q[HEAD_DIM], *logit, mx, z;
     if (err) {
@@ -413,6 +423,16 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
         return err;
     }
     n = L + i + 1; /* keys 0 .. L + i */
+    /* window key L + j is seen when j <= i (causal), or, with a draft tree,
+     * when window slot j is i or one of its ancestors */
+    for (j = 0; j < MAX_WINDOW; ++j)
+        seen[j] = J->parent == NULL && j <= i;
+    if (J->parent != NULL)
+        for (j = i;; j = J->parent[(size_t)b * J->window + j]) {
+            seen[j] = 1;
+            if (j == 0)
+                break;
+        }
     qrow = J->q + (((size_t)b * J->window + i) * J->num_q_heads + h) * HEAD_DIM;
     for (d = 0; d < HEAD_DIM; ++d)
         q[d] = (double)bf16_value(qrow[d]);
@@ -420,6 +440,8 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
     mx = -INFINITY;
     for (j = 0; j < n; ++j) {
         double s = 0.0;
+        if (j >= L && !seen[j - L])
+            continue;
         for (d = 0; d < HEAD_DIM; ++d)
             s += q[d] * cache_value(c, 0, row, hk, j, d);
         logit[j] = J->sm_scale * s;
@@ -430,7 +452,10 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
         o[d] = 0.0;
     z = 0.0;
     for (j = 0; j < n; ++j) {
-        double p = exp(logit[j] - mx);
+        double p;
+        if (j >= L && !seen[j - L])
+            continue;
+        p = exp(logit[j] - mx);
         z += p;
         for (d = 0; d < HEAD_DIM; ++d)
             o[d] += p * cache_value(c, 1, row, hk, j, d);
@@ -506,6 +531,60 @@ int oracle_verify_attn(int dtype, int num_pages, int num_kv_heads, const uint8_t
     J.out = out;
     J.rows = rows;
     J.nrows = nrows;
+    pthread_mutex_init(&J.lock, NULL);
+    if (threads < 1)
+        threads = 1;
+    if (threads > 256)
+        threads = 256;
+    if (threads == 1) {
+        verify_worker(&J);
+    } else {
+        for (t = 0; t < threads; ++t)
+            pthread_create(&tid[t], NULL, verify_worker, &J);
+        for (t = 0; t < threads; ++t)
+            pthread_join(tid[t], NULL);
+    }
+    pthread_mutex_destroy(&J.lock);
+    if (status)
+        *status |= J.status;
+    return 0;
+}
+
+/* Draft-tree attention (R9): as oracle_verify_attn, but window row i sees
+ * the window keys of its ancestors and itself only.  parent [B][W] with
+ * 0 <= parent[b][i] < i for i >= 1 (entry 0 unused); window <= 16. */
+int oracle_tree_attn(int dtype, int num_pages, int num_kv_heads, const uint8_t* k_codes, const uint8_t* v_codes,
+                     const void* k_scales, const void* v_scales, const uint16_t* q, int num_q_heads, int num_lanes,
+                     int window, const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                     const int32_t* parent, float sm_scale, double* out, int threads, int32_t* status)
+{
+    verify_job J;
+    int t, b, i;
+    pthread_t tid[256];
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || window > MAX_WINDOW || parent == NULL)
+        return -1;
+    for (b = 0; b < num_lanes; ++b)
+        for (i = 1; i < window; ++i)
+            if (parent[(size_t)b * window + i] < 0 || parent[(size_t)b * window + i] >= i)
+                return -1;
+    memset(&J, 0, sizeof J);
+    J.c.dtype = dtype;
+    J.c.num_pages = num_pages;
+    J.c.num_kv_heads = num_kv_heads;
+    J.c.k_codes = (uint8_t*)k_codes;
+    J.c.v_codes = (uint8_t*)v_codes;
+    J.c.k_scales = (void*)k_scales;
+    J.c.v_scales = (void*)v_scales;
+    J.q = q;
+    J.num_q_heads = num_q_heads;
+    J.num_lanes = num_lanes;
+    J.window = window;
+    J.max_pages = max_pages;
+    J.page_table = page_table;
+    J.seq_lens = seq_lens;
+    J.sm_scale = (double)sm_scale;
+    J.out = out;
+    J.parent = parent;
     pthread_mutex_init(&J.lock, NULL);
     if (threads < 1)
         threads = 1;
@@ -721,5 +800,62 @@ int oracle_spec_accept_sampled(const float* logits, const float* draft_probs, in
     }
     free(p);
     free(w);
+    return 0;
+}
+
+/* Draft-tree acceptance (R9).  tokens [B][W]: the window's tokens (slot 0,
+ * the root, is not checked); parent [B][W] as for oracle_tree_attn.
+ * path [B][W] (out): the accepted slots, root first, then -1;
+ * out_tokens [B][W] (out): the accepted tokens after the root, then the
+ * bonus token, then -1; accept_len [B] = the accepted nodes after the root;
+ * the commit adds 1 + a.  A lane with an invalid parent sets bit 32 and gets
+ * a = 0, path and tokens -1, no commit.  Token ids outside [0, vocab) set the
+ * draft bit and never match. */
+int oracle_tree_accept(const float* logits, int num_lanes, int window, int vocab, const int32_t* tokens,
+                       const int32_t* parent, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                       int32_t* seq_lens_inout, int32_t* status)
+{
+    int b, i, c;
+    for (b = 0; b < num_lanes; ++b) {
+        const int32_t* par = parent + (size_t)b * window;
+        const int32_t* tk = tokens + (size_t)b * window;
+        int32_t* pa = path + (size_t)b * window;
+        int32_t* ot = out_tokens + (size_t)b * window;
+        int bad = 0, a = 0, n = 0;
+        for (i = 0; i < window; ++i) {
+            pa[i] = -1;
+            ot[i] = -1;
+        }
+        for (i = 1; i < window; ++i) {
+            if (par[i] < 0 || par[i] >= i)
+                bad = 1;
+            if ((tk[i] < 0 || tk[i] >= vocab) && status)
+                *status |= ST_BAD_DRAFT;
+        }
+        if (bad) {
+            accept_len[b] = 0;
+            if (status)
+                *status |= 32;
+            continue;
+        }
+        pa[0] = 0;
+        for (;;) {
+            int t = oracle_argmax(logits + ((size_t)b * window + n) * vocab, vocab), next = -1;
+            for (c = n + 1; c < window && next < 0; ++c)
+                if (par[c] == n && tk[c] == t)
+                    next = c;
+            if (next < 0) {
+                ot[a] = t;
+                break;
+            }
+            ot[a] = tk[next];
+            ++a;
+            pa[a] = next;
+            n = next;
+        }
+        accept_len[b] = a;
+        if (seq_lens_inout)
+            seq_lens_inout[b] += 1 + a;
+    }
     return 0;
 }
