@@ -21,6 +21,7 @@
  *                       prefix, optional commit of the new lengths
  *   spec_accept_lazy -- the same acceptance reading each lane's rows only up
  *                       to its first disagreement, with per-lane draft counts
+ *   spec_accept_tree -- greedy acceptance of a tree of drafted tokens
  *   spec_accept_sampled -- lossless stochastic acceptance with the draft
  *                       distribution (ratio test, residual draw)
  *
@@ -110,6 +111,7 @@ typedef struct {
 #define SDVA_STATUS_BAD_DRAFT 4 /* a draft id is outside [0, vocab) */
 #define SDVA_STATUS_TIMEOUT 8   /* a bounded device wait gave up */
 #define SDVA_STATUS_BAD_COUNT 16 /* a per-lane draft or token count is out of range */
+#define SDVA_STATUS_BAD_TREE 32 /* a draft tree's parent is not an earlier slot */
 
 /*
  * kv_append_quant -- write tokens [L_b, L_b + n_new) of every lane into the
@@ -268,6 +270,34 @@ int spec_accept(const float* logits, int num_lanes, int window, int vocab, const
 int spec_accept_lazy(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
                      const int32_t* num_drafts, int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout,
                      int32_t* status, sdva_stream_t stream);
+
+/*
+ * spec_accept_tree -- greedy acceptance of a draft tree.
+ *   The pages verify chains of drafts (Baseten talk summary, section
+ *   "추측 디코드"); a tree of candidates is this library's reading of the
+ *   same check: window slot 0 is the root (the last committed token) and
+ *   slot i >= 1 hangs under parent[b][i] < i.  From the root, the walk moves
+ *   to the first child (in slot order) whose token is the argmax of the
+ *   current node's logits row, and stops when no child agrees.
+ *   logits    : fp32 [num_lanes][window][vocab]; row i scores the token that
+ *               follows slot i.
+ *   tokens    : int32 [num_lanes][window]: the window's tokens (slot 0 is
+ *               not read); parent: int32 [num_lanes][window] (slot 0 not
+ *               read).  Both nullable when window == 1.
+ *   accept_len: int32 [num_lanes] (out): a, the nodes accepted after the root.
+ *   path      : int32 [num_lanes][window] (out): the accepted slots, root
+ *               (0) first, -1 after; also used as scratch by the call.
+ *   out_tokens: int32 [num_lanes][window] (out): the accepted tokens, then
+ *               the bonus token (argmax of the last node's row), -1 after.
+ *   seq_lens_inout: nullable: adds 1 + a.
+ * Argmax ties go to the lowest index, NaN never wins (as spec_accept).  A
+ * lane with a parent outside [0, i) sets SDVA_STATUS_BAD_TREE and gets a = 0,
+ * path and out_tokens all -1, no commit.  A token outside [0, vocab) sets
+ * SDVA_STATUS_BAD_DRAFT and never matches.  Limits as spec_accept.
+ */
+int spec_accept_tree(const float* logits, int num_lanes, int window, int vocab, const int32_t* tokens,
+                     const int32_t* parent, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                     int32_t* seq_lens_inout, int32_t* status, sdva_stream_t stream);
 
 /*
  * spec_accept_sampled -- lossless stochastic acceptance of a verify window

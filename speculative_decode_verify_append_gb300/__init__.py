@@ -14,6 +14,8 @@ The calls mirror ``include/sdva.h``:
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
     spec_accept_lazy(logits, drafts, accept_len, out_tokens, num_drafts=None, seq_lens_inout=None, status=None,
                      stream=None)
+    spec_accept_tree(logits, tokens, parent, accept_len, path, out_tokens, seq_lens_inout=None, status=None,
+                     stream=None)
     spec_accept_sampled_workspace_size(num_lanes, window)
     spec_accept_sampled(logits, draft_probs, drafts, u_accept, u_sample, accept_len, out_tokens, workspace,
                         seq_lens_inout=None, status=None, stream=None)
@@ -45,6 +47,7 @@ STATUS_OVERFLOW = 2
 STATUS_BAD_DRAFT = 4
 STATUS_TIMEOUT = 8
 STATUS_BAD_COUNT = 16
+STATUS_BAD_TREE = 32
 LAZY_WALK_MIN_LANES = 48  # SDVA_LAZY_WALK_MIN_LANES: spec_accept_lazy walks rows from this many lanes on
 
 if not os.path.exists(LIB_PATH):
@@ -87,6 +90,8 @@ _lib.spec_accept.restype = _I
 _lib.spec_accept.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
 _lib.spec_accept_lazy.restype = _I
 _lib.spec_accept_lazy.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+_lib.spec_accept_tree.restype = _I
+_lib.spec_accept_tree.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.spec_accept_sampled_workspace_size.restype = ctypes.c_size_t
 _lib.spec_accept_sampled_workspace_size.argtypes = [_I, _I]
 _lib.spec_accept_sampled.restype = _I
@@ -95,7 +100,7 @@ _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
-            "spec_accept_lazy", "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
+            "spec_accept_lazy", "spec_accept_tree", "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -267,6 +272,23 @@ def spec_accept_lazy(logits: torch.Tensor, drafts: torch.Tensor | None, accept_l
                                _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"),
                                _dptr(status, torch.int32, "status"), _stream(stream))
     _check("spec_accept_lazy", rc)
+
+
+def spec_accept_tree(logits: torch.Tensor, tokens: torch.Tensor | None, parent: torch.Tensor | None,
+                     accept_len: torch.Tensor, path: torch.Tensor, out_tokens: torch.Tensor,
+                     seq_lens_inout: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """logits fp32 [B][W][V]; tokens, parent int32 [B][W]; accept_len int32 [B];
+    path, out_tokens int32 [B][W]."""
+    B, W, V = logits.shape
+    rc = _lib.spec_accept_tree(_dptr(logits, torch.float32, "logits"), B, W, V,
+                               _dptr(tokens, torch.int32, "tokens") if W > 1 else None,
+                               _dptr(parent, torch.int32, "parent") if W > 1 else None,
+                               _dptr(accept_len, torch.int32, "accept_len"), _dptr(path, torch.int32, "path"),
+                               _dptr(out_tokens, torch.int32, "out_tokens"),
+                               _dptr(seq_lens_inout, torch.int32, "seq_lens_inout"),
+                               _dptr(status, torch.int32, "status"), _stream(stream))
+    _check("spec_accept_tree", rc)
 
 
 def spec_accept_sampled_workspace_size(num_lanes: int, window: int) -> int:

@@ -21,6 +21,8 @@ extern "C" const char* sdva_status_string(int code) {
       return "device status: a draft id is outside [0, vocab)";
     case SDVA_STATUS_TIMEOUT:
       return "device status: a bounded device wait timed out";
+    case SDVA_STATUS_BAD_TREE:
+      return "device status: a draft tree's parent is not an earlier slot";
     case SDVA_STATUS_BAD_COUNT:
       return "device status: a per-lane draft or token count is out of range";
     default:

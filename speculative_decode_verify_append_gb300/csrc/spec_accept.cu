@@ -310,6 +310,65 @@ __global__ void __launch_bounds__(128) accept_lazy_finalize_kernel(int num_lanes
   }
 }
 
+// Draft-tree acceptance, one warp per lane (lane i of the warp holds window
+// slot i): the argmax kernel has left row i's argmax in path[b][i].  From the
+// root, the walk moves to the lowest slot c whose parent is the current node
+// and whose token is the current node's argmax; a = the nodes accepted, the
+// bonus = the last node's argmax.  Programmatic dependent of the argmax kernel.
+__global__ void __launch_bounds__(128) accept_tree_finalize_kernel(int num_lanes, int window, int vocab,
+                                                                   const int32_t* tokens, const int32_t* parent,
+                                                                   int32_t* path, int32_t* out_tokens,
+                                                                   int32_t* accept_len, int32_t* seq_lens,
+                                                                   int32_t* status) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (b >= num_lanes) return;
+  const bool in = lane < window;
+  const size_t base = (size_t)b * window;
+  const int am = in ? path[base + lane] : -1;
+  const int par = in && lane > 0 ? parent[base + lane] : -1;
+  const int tk = in && lane > 0 ? tokens[base + lane] : -1;
+  const bool bad_parent = in && lane > 0 && (par < 0 || par >= lane);
+  const bool bad_token = in && lane > 0 && (tk < 0 || tk >= vocab);
+  const unsigned any_bad_parent = __ballot_sync(0xffffffffu, bad_parent);
+  const unsigned any_bad_token = __ballot_sync(0xffffffffu, bad_token);
+  if (any_bad_parent) {
+    if (in) {
+      path[base + lane] = -1;
+      out_tokens[base + lane] = -1;
+    }
+    if (lane == 0) {
+      accept_len[b] = 0;
+      raise_status(status, SDVA_STATUS_BAD_TREE | (any_bad_token ? SDVA_STATUS_BAD_DRAFT : 0));
+    }
+    return;
+  }
+  int n = 0, a = 0, my_path = lane == 0 ? 0 : -1, my_tok = -1;
+  for (int step = 0; step < window; ++step) {
+    const int t = __shfl_sync(0xffffffffu, am, n);
+    const unsigned next = __ballot_sync(0xffffffffu, in && lane > n && par == n && tk == t);
+    if (next == 0u) {
+      if (lane == a) my_tok = t;  // the bonus token
+      break;
+    }
+    const int c = __ffs(next) - 1;  // the first child in slot order
+    const int tc = __shfl_sync(0xffffffffu, tk, c);
+    if (lane == a) my_tok = tc;  // the a-th accepted token
+    ++a;
+    if (lane == a) my_path = c;
+    n = c;
+  }
+  if (in) {
+    path[base + lane] = lane <= a ? my_path : -1;
+    out_tokens[base + lane] = lane <= a ? my_tok : -1;
+  }
+  if (lane == 0) {
+    accept_len[b] = a;
+    if (seq_lens != nullptr) seq_lens[b] += 1 + a;
+    if (any_bad_token) raise_status(status, SDVA_STATUS_BAD_DRAFT);
+  }
+}
+
 }  // namespace
 }  // namespace sdva
 
@@ -419,4 +478,19 @@ extern "C" int spec_accept_lazy(const float* logits, int num_lanes, int window, 
                          seq_lens_inout, status) != cudaSuccess)
     return SDVA_ERR_CUDA;
   return SDVA_OK;
+}
+
+extern "C" int spec_accept_tree(const float* logits, int num_lanes, int window, int vocab, const int32_t* tokens,
+                                const int32_t* parent, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                                int32_t* seq_lens_inout, int32_t* status, sdva_stream_t stream) {
+  if (logits == nullptr || accept_len == nullptr || path == nullptr || out_tokens == nullptr) return SDVA_ERR_INVALID;
+  if (num_lanes <= 0 || window <= 0 || vocab <= 0) return SDVA_ERR_INVALID;
+  if (window > 1 && (tokens == nullptr || parent == nullptr)) return SDVA_ERR_INVALID;
+  if (window > kMaxWindow) return SDVA_ERR_UNSUPPORTED;
+  if ((long long)num_lanes * window > 65535) return SDVA_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the row argmaxes go to `path` first; the walk overwrites them
+  if (const int rc = launch_argmax_rows(logits, num_lanes, window, vocab, nullptr, path, s)) return rc;
+  return launch_finalize(accept_tree_finalize_kernel, num_lanes, s, num_lanes, window, vocab, tokens, parent, path,
+                         out_tokens, accept_len, seq_lens_inout, status);
 }

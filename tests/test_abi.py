@@ -74,7 +74,7 @@ def test_status_strings(lib):
     f = lib.sdva_status_string
     f.restype = ctypes.c_char_p
     f.argtypes = [ctypes.c_int]
-    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 16, 3, -99):
+    for code in (0, -1, -2, -3, -4, 1, 2, 4, 8, 16, 32, 3, -99):
         s = f(code)
         assert s and len(s) >= 2
 
@@ -136,6 +136,11 @@ def test_argument_validation_returns_before_cuda(lib):
     assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, fake, 8, None, None) == -3  # too small
     assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, None, 4096, None, None) == -3
     assert sm(fake, fake, 2, 4, 100, fake, fake, fake, fake, fake, None, P(0x1004), 4096, None, None) == -3
+    tr = lib.spec_accept_tree
+    tr.restype = ctypes.c_int
+    assert tr(fake, 2, 4, 100, None, fake, fake, fake, fake, None, None, None) == -1  # tokens needed
+    assert tr(fake, 2, 4, 100, fake, fake, fake, None, fake, None, None, None) == -1  # path needed
+    assert tr(fake, 2, 17, 100, fake, fake, fake, fake, fake, None, None, None) == -2
     lz = lib.spec_accept_lazy
     lz.restype = ctypes.c_int
     assert lz(fake, 1, 4, 100, None, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
@@ -151,5 +156,6 @@ def test_header_constants_match_the_binding(lib):
     import speculative_decode_verify_append_gb300 as sdva
     assert int(defs["SDVA_LAZY_WALK_MIN_LANES"]) == sdva.LAZY_WALK_MIN_LANES
     assert int(defs["SDVA_STATUS_BAD_COUNT"]) == sdva.STATUS_BAD_COUNT
+    assert int(defs["SDVA_STATUS_BAD_TREE"]) == sdva.STATUS_BAD_TREE
     assert int(defs["SDVA_STATUS_BAD_DRAFT"]) == sdva.STATUS_BAD_DRAFT
     assert int(defs["SDVA_ERR_WORKSPACE"]) == sdva.ERR_WORKSPACE
