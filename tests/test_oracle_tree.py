@@ -175,3 +175,38 @@ def test_invalid_tree_is_refused():
     spec, step, cache = _cache_with_window(oracle.KV_FP8, 94, L, W, H, Hq)
     with pytest.raises(ValueError):
         oracle.tree_attn(cache, step.q, step.page_table, step.seq_lens, np.array([[0, 0, 2, 1]], np.int32), 0.1)
+
+
+def test_compaction_by_ragged_reappend_int4():
+    # after acceptance the path's K/V must sit at L + 1 .. L + a: re-appending the
+    # accepted slots' rows there (a ragged append of a tokens) leaves, with INT4's
+    # per-token scales, exactly what appending the accepted chain directly leaves
+    rng = np.random.default_rng(95)
+    L, W, H = 100, 8, 2
+    spec = synth.Spec("tree", 95, 1, 0, 0, 2 * H, H, W, oracle.KV_INT4, 64, 0.7, True)
+    step = synth.make_step(spec, seq_lens=np.array([L], np.int32), with_accept=False)
+    parent = np.array([[0, 0, 1, 0, 2, 4, 3, 5]], np.int32)
+    path = [0, 1, 2, 4, 5]  # an accepted path of the tree, a = 4
+    a = len(path) - 1
+
+    def fresh():
+        c = oracle.Cache(oracle.KV_INT4, step.num_pages, H)
+        for start, n in synth.fill_chunks(L, 64):
+            k, v = synth.context_chunk(spec, 0, start, n)
+            oracle.append(c, k[None], v[None], step.page_table, np.array([start], np.int32))
+        return c
+
+    tree = fresh()
+    assert oracle.append(tree, step.k_win, step.v_win, step.page_table, step.seq_lens) == 0
+    kg = np.ascontiguousarray(step.k_win[:, path[1:]])
+    vg = np.ascontiguousarray(step.v_win[:, path[1:]])
+    pad = np.zeros((1, W - 1 - a) + kg.shape[2:], kg.dtype)
+    assert oracle.append_ragged(tree, np.concatenate([kg, pad], 1), np.concatenate([vg, pad], 1), step.page_table,
+                                step.seq_lens + 1, np.array([a], np.int32)) == 0
+    chain = fresh()
+    assert oracle.append(chain, step.k_win[:, path], step.v_win[:, path], step.page_table, step.seq_lens) == 0
+    row = step.page_table[0]
+    for pos in range(L + a + 1):
+        pid, off = row[pos // PAGE], pos % PAGE
+        for n in ("k_codes", "v_codes", "k_scales", "v_scales"):
+            assert np.array_equal(getattr(tree, n)[pid, :, off], getattr(chain, n)[pid, :, off]), (pos, n)
