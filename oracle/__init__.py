@@ -27,6 +27,8 @@ _lock = threading.Lock()
 
 KV_FP8 = 0
 KV_INT4 = 1
+KV_INT8 = 2      # INT8 group-64 (fp16 scales), oracle only
+KV_FP8_ROW = 3   # FP8 E4M3 with one fp32 scale per (token, head) row, oracle only
 PAGE = 64
 HEAD_DIM = 128
 
@@ -61,6 +63,10 @@ def _load():
             lib.oracle_f16_encode.argtypes = [ctypes.c_float]
             lib.oracle_int4_group.restype = ctypes.c_uint16
             lib.oracle_int4_group.argtypes = [P, I, P]
+            lib.oracle_int8_group.restype = ctypes.c_uint16
+            lib.oracle_int8_group.argtypes = [P, I, P]
+            lib.oracle_fp8_row.restype = ctypes.c_float
+            lib.oracle_fp8_row.argtypes = [P, I, P]
             lib.oracle_append.restype = I
             lib.oracle_append.argtypes = [I, I, I, P, P, P, P, P, P, I, I, P, I, P, P]
             lib.oracle_verify_attn.restype = I
@@ -121,6 +127,22 @@ def int4_group(x) -> tuple[int, np.ndarray]:
     return s, codes
 
 
+def int8_group(x) -> tuple[int, np.ndarray]:
+    """INT8 group codec: (fp16 scale bits, codes in [-127, 127])."""
+    x = _as(x, np.float32)
+    codes = np.zeros(x.size, np.int8)
+    s = _load().oracle_int8_group(_ptr(x), x.size, _ptr(codes))
+    return s, codes
+
+
+def fp8_row(x) -> tuple[float, np.ndarray]:
+    """FP8 row codec: (fp32 scale, E4M3 codes)."""
+    x = _as(x, np.float32)
+    codes = np.zeros(x.size, np.uint8)
+    s = _load().oracle_fp8_row(_ptr(x), x.size, _ptr(codes))
+    return float(np.float32(s)), codes
+
+
 # --------------------------------------------------------------------------
 # the cache
 # --------------------------------------------------------------------------
@@ -129,6 +151,8 @@ class Cache:
 
     FP8:  codes uint8 [pages][Hkv][64][128], scales float32 [pages][Hkv]
     INT4: codes uint8 [pages][Hkv][64][64],  scales uint16 (fp16 bits) [pages][Hkv][64][4]
+    INT8: codes uint8 (int8 bits) [pages][Hkv][64][128], scales uint16 (fp16 bits) [pages][Hkv][64][2]
+    FP8_ROW: codes uint8 [pages][Hkv][64][128], scales float32 [pages][Hkv][64]
     """
 
     def __init__(self, dtype: int, num_pages: int, num_kv_heads: int):
@@ -138,6 +162,12 @@ class Cache:
         if dtype == KV_FP8:
             shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
             sshape, sdt = (num_pages, num_kv_heads), np.float32
+        elif dtype == KV_INT8:
+            shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
+            sshape, sdt = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 64), np.uint16
+        elif dtype == KV_FP8_ROW:
+            shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
+            sshape, sdt = (num_pages, num_kv_heads, PAGE), np.float32
         else:
             shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 2)
             sshape, sdt = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 32), np.uint16

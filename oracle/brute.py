@@ -67,6 +67,26 @@ def f16_value(bits: int) -> float:
     return struct.unpack("<e", struct.pack("<H", bits))[0]
 
 
+def int_group(xs, qmax):
+    """Symmetric group codec to [-qmax, qmax]: the fp16 scale of amax / qmax,
+    codes = x / s rounded half to even and clamped.  Returns (scale bits, codes)."""
+    amax = max(abs(x) for x in xs)
+    t = min(f32(amax / qmax), 65504.0)
+    s_bits = f16_bits(t)
+    s = f16_value(s_bits)
+    if s == 0.0:
+        return s_bits, [0] * len(xs)
+    return s_bits, [max(-qmax, min(qmax, round(f32(x / s)))) for x in xs]
+
+
+def fp8_row(xs):
+    """Row codec: one fp32 scale amax / 448, codes E4M3 of x / s.  Returns (scale, codes)."""
+    s = f32(max(abs(x) for x in xs) / 448.0)
+    if s == 0.0:
+        return s, [0] * len(xs)
+    return s, [e4m3_encode(f32(x / s)) for x in xs]
+
+
 def int4_group(xs):
     amax = max(abs(x) for x in xs)
     t = f32(amax / 7.0)
@@ -97,6 +117,10 @@ class Cache:
     def value(self, kv: int, pid: int, h: int, off: int, d: int) -> float:
         if self.dtype == 0:
             return e4m3_value(self.codes[kv][(pid, h, off)][d]) * self.scales[kv][(pid, h)]
+        if self.dtype == 2:
+            return self.codes[kv][(pid, h, off)][d] * f16_value(self.scales[kv][(pid, h, off)][d // 64])
+        if self.dtype == 3:
+            return e4m3_value(self.codes[kv][(pid, h, off)][d]) * self.scales[kv][(pid, h, off)]
         return self.codes[kv][(pid, h, off)][d] * f16_value(self.scales[kv][(pid, h, off)][d // 32])
 
 
@@ -106,6 +130,22 @@ def append(cache: Cache, new_rows, page_row, L: int):
     H = len(new_rows[0][0]) if n else 0
     for kv in (0, 1):
         for h in range(H):
+            if cache.dtype in (2, 3):
+                for t in range(n):
+                    pos = L + t
+                    pid, off = page_row[pos // PAGE], pos % PAGE
+                    xs = [bf16(b) for b in new_rows[kv][t][h]]
+                    if cache.dtype == 2:
+                        scales, codes = [], []
+                        for g in range(2):
+                            sc, c = int_group(xs[64 * g:64 * g + 64], 127)
+                            scales.append(sc)
+                            codes.extend(c)
+                    else:
+                        scales, codes = fp8_row(xs)
+                    cache.codes[kv][(pid, h, off)] = codes
+                    cache.scales[kv][(pid, h, off)] = scales
+                continue
             if cache.dtype == 1:
                 for t in range(n):
                     pos = L + t

@@ -47,6 +47,14 @@
  *      drafts only drafts[b][0 .. d_b) are compared, and the rows after the
  *      first disagreement decide nothing, so the lazy form reports argmaxes
  *      only for rows 0 .. a and -1 after them.
+ *   R10 INT8 group-64 KV (the NInfer review, section "성능과 평가", names
+ *      "INT8 group-64" only): like R3 with 127 in place of 7 and groups of 64
+ *      head dims: s = fp16_rne(min(amax / 127, 65504)), q = clamp(rint(x /
+ *      s), -127, 127), halves to even, two's complement bytes.
+ *   R11 FP8 E4M3 row KV (the same section names "FP8 E4M3 row-256", 256
+ *      being the head size of the model measured): one fp32 scale per
+ *      (token, kv head) row, s = amax / 448, codes e4m3_rne_sat(x / s).
+ *      Every token carries its own scale, so nothing is re-encoded.
  *   R9 Draft trees (a reading: the pages describe chains of drafts only):
  *      window slot 0 is the root (the last committed token) and slot i >= 1
  *      has a parent slot parent[i] < i; the window is appended in slot order
@@ -79,7 +87,7 @@
 #define MAX_WINDOW 16
 
 enum { ST_BAD_PAGE = 1, ST_OVERFLOW = 2, ST_BAD_DRAFT = 4, ST_BAD_COUNT = 16 };
-enum { KV_FP8 = 0, KV_INT4 = 1 };
+enum { KV_FP8 = 0, KV_INT4 = 1, KV_INT8 = 2, KV_FP8_ROW = 3 };
 
 /* ------------------------------------------------------------------ */
 /* bf16 input values                                                    */
@@ -200,9 +208,9 @@ uint16_t oracle_f16_encode(float x)
 /* ------------------------------------------------------------------ */
 /* INT4 group codec (R3)                                                */
 /* ------------------------------------------------------------------ */
-/* Quantise one group of n values; returns the fp16 scale bits and writes
- * codes in [-7, 7]. */
-uint16_t oracle_int4_group(const float* x, int n, int8_t* codes)
+/* Quantise one group of n values symmetrically to [-qmax, qmax]; returns
+ * the fp16 scale bits (R3 with qmax 7, R10 with qmax 127). */
+static uint16_t int_group(const float* x, int n, int qmax, int8_t* codes)
 {
     float amax = 0.0f, t, sf;
     uint16_t s16;
@@ -212,7 +220,7 @@ uint16_t oracle_int4_group(const float* x, int n, int8_t* codes)
         if (a > amax)
             amax = a;
     }
-    t = amax / 7.0f; /* IEEE fp32 division */
+    t = amax / (float)qmax; /* IEEE fp32 division */
     if (t > 65504.0f)
         t = 65504.0f;
     s16 = oracle_f16_encode(t);
@@ -223,14 +231,39 @@ uint16_t oracle_int4_group(const float* x, int n, int8_t* codes)
         } else {
             float r = x[i] / sf; /* IEEE fp32 division */
             double k = nearbyint((double)r);
-            if (k > 7.0)
-                k = 7.0;
-            if (k < -7.0)
-                k = -7.0;
+            if (k > (double)qmax)
+                k = (double)qmax;
+            if (k < -(double)qmax)
+                k = -(double)qmax;
             codes[i] = (int8_t)k;
         }
     }
     return s16;
+}
+
+/* Quantise one group of n values; returns the fp16 scale bits and writes
+ * codes in [-7, 7]. */
+uint16_t oracle_int4_group(const float* x, int n, int8_t* codes) { return int_group(x, n, 7, codes); }
+
+/* INT8 group codec (R10): codes in [-127, 127], fp16 scale. */
+uint16_t oracle_int8_group(const float* x, int n, int8_t* codes) { return int_group(x, n, 127, codes); }
+
+/* FP8 row codec (R11): one fp32 scale amax / 448 for the n values of a row;
+ * codes e4m3(x / s) (round to nearest even, saturating); a zero scale gives
+ * zero codes.  Returns the scale. */
+float oracle_fp8_row(const float* x, int n, uint8_t* codes)
+{
+    float amax = 0.0f, s;
+    int i;
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax)
+            amax = a;
+    }
+    s = amax / 448.0f; /* IEEE fp32 division */
+    for (i = 0; i < n; ++i)
+        codes[i] = s == 0.0f ? 0x00 : oracle_e4m3_encode(x[i] / s);
+    return s;
 }
 
 static int int4_nibble_value(uint8_t byte, int high)
@@ -243,12 +276,14 @@ static int int4_nibble_value(uint8_t byte, int high)
 /* The cache                                                            */
 /* ------------------------------------------------------------------ */
 typedef struct {
-    int dtype; /* KV_FP8 or KV_INT4 */
+    int dtype; /* KV_FP8, KV_INT4, KV_INT8 or KV_FP8_ROW */
     int num_pages;
     int num_kv_heads;
-    uint8_t* k_codes; /* FP8: [pages][Hkv][64][128]; INT4: [pages][Hkv][64][64] */
+    uint8_t* k_codes; /* FP8, INT8, FP8_ROW: [pages][Hkv][64][128]; INT4: [pages][Hkv][64][64] */
     uint8_t* v_codes;
-    void* k_scales; /* FP8: float [pages][Hkv]; INT4: uint16 (fp16) [pages][Hkv][64][4] */
+    /* FP8: float [pages][Hkv]; INT4: uint16 (fp16) [pages][Hkv][64][4];
+     * INT8: uint16 (fp16) [pages][Hkv][64][2]; FP8_ROW: float [pages][Hkv][64] */
+    void* k_scales;
     void* v_scales;
 } oracle_cache;
 
@@ -278,6 +313,14 @@ static double cache_value(const oracle_cache* c, int is_v, const int32_t* row, i
         const float* sc = (const float*)(is_v ? c->v_scales : c->k_scales);
         uint8_t code = codes[(ph * PAGE + off) * HEAD_DIM + d];
         return oracle_e4m3_decode(code) * (double)sc[ph];
+    } else if (c->dtype == KV_FP8_ROW) {
+        const float* sc = (const float*)(is_v ? c->v_scales : c->k_scales);
+        uint8_t code = codes[(ph * PAGE + off) * HEAD_DIM + d];
+        return oracle_e4m3_decode(code) * (double)sc[ph * PAGE + off];
+    } else if (c->dtype == KV_INT8) {
+        const uint16_t* sc = (const uint16_t*)(is_v ? c->v_scales : c->k_scales);
+        int8_t q = (int8_t)codes[(ph * PAGE + off) * HEAD_DIM + d];
+        return (double)q * oracle_f16_decode(sc[(ph * PAGE + off) * (HEAD_DIM / 64) + d / 64]);
     } else {
         const uint16_t* sc = (const uint16_t*)(is_v ? c->v_scales : c->k_scales);
         uint8_t byte = codes[(ph * PAGE + off) * (HEAD_DIM / 2) + d / 2];
@@ -344,6 +387,29 @@ static void append_int4_token(const oracle_cache* c, int is_v, int pid, int h, i
     }
 }
 
+/* INT8 group-64 and FP8 row formats: every token carries its own scales. */
+static void append_token_rowscaled(const oracle_cache* c, int is_v, int pid, int h, int off, const uint16_t* src)
+{
+    size_t ph = (size_t)pid * c->num_kv_heads + h;
+    uint8_t* codes = (is_v ? c->v_codes : c->k_codes) + (ph * PAGE + off) * HEAD_DIM;
+    float x[HEAD_DIM];
+    int i, g;
+    for (i = 0; i < HEAD_DIM; ++i)
+        x[i] = bf16_value(src[i]);
+    if (c->dtype == KV_FP8_ROW) {
+        float* scales = (float*)(is_v ? c->v_scales : c->k_scales);
+        scales[ph * PAGE + off] = oracle_fp8_row(x, HEAD_DIM, codes);
+    } else {
+        uint16_t* scales = (uint16_t*)(is_v ? c->v_scales : c->k_scales) + (ph * PAGE + off) * (HEAD_DIM / 64);
+        for (g = 0; g < HEAD_DIM / 64; ++g) {
+            int8_t q[64];
+            scales[g] = oracle_int8_group(x + 64 * g, 64, q);
+            for (i = 0; i < 64; ++i)
+                codes[64 * g + i] = (uint8_t)q[i];
+        }
+    }
+}
+
 /* Writes tokens [L_b, L_b + n_new) of every lane.  Lanes whose range does
  * not fit or touches an invalid page id are skipped and flagged. */
 int oracle_append(int dtype, int num_pages, int num_kv_heads, uint8_t* k_codes, uint8_t* v_codes,
@@ -376,9 +442,13 @@ int oracle_append(int dtype, int num_pages, int num_kv_heads, uint8_t* k_codes, 
                     }
                 } else {
                     int t;
-                    for (t = L; t < L + n_new; ++t)
-                        append_int4_token(&c, kv, row[t / PAGE], h, t % PAGE,
-                                          lane_src + (size_t)(t - L) * token_stride + h * HEAD_DIM);
+                    for (t = L; t < L + n_new; ++t) {
+                        const uint16_t* src = lane_src + (size_t)(t - L) * token_stride + h * HEAD_DIM;
+                        if (dtype == KV_INT4)
+                            append_int4_token(&c, kv, row[t / PAGE], h, t % PAGE, src);
+                        else
+                            append_token_rowscaled(&c, kv, row[t / PAGE], h, t % PAGE, src);
+                    }
                 }
             }
         }
