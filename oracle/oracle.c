@@ -51,9 +51,10 @@
  *      "INT8 group-64" only): like R3 with 127 in place of 7 and groups of 64
  *      head dims: s = fp16_rne(min(amax / 127, 65504)), q = clamp(rint(x /
  *      s), -127, 127), halves to even, two's complement bytes.
- *   R11 FP8 E4M3 row KV (the same section names "FP8 E4M3 row-256", 256
- *      being the head size of the model measured): one fp32 scale per
- *      (token, kv head) row, s = amax / 448, codes e4m3_rne_sat(x / s).
+ *   R11 FP8 E4M3 row KV (the same section names "FP8 E4M3 row-256" only;
+ *      read as one scale per row of a token's head, 128 dims here): one fp32
+ *      scale per (token, kv head) row, s = amax / 448, codes
+ *      e4m3_rne_sat(x / s).
  *      Every token carries its own scale, so nothing is re-encoded.
  *   R9 Draft trees (a reading: the pages describe chains of drafts only):
  *      window slot 0 is the root (the last committed token) and slot i >= 1
