@@ -494,16 +494,17 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
         return err;
     }
     n = L + i + 1; /* keys 0 .. L + i */
-    /* window key L + j is seen when j <= i (causal), or, with a draft tree,
-     * when window slot j is i or one of its ancestors */
-    for (j = 0; j < MAX_WINDOW; ++j)
-        seen[j] = J->parent == NULL && j <= i;
-    if (J->parent != NULL)
+    /* keys 0 .. L + i are the causal window; with a draft tree (window <= 16)
+     * window key L + j is seen only when slot j is i or one of its ancestors */
+    if (J->parent != NULL) {
+        for (j = 0; j < MAX_WINDOW; ++j)
+            seen[j] = 0;
         for (j = i;; j = J->parent[(size_t)b * J->window + j]) {
             seen[j] = 1;
             if (j == 0)
                 break;
         }
+    }
     qrow = J->q + (((size_t)b * J->window + i) * J->num_q_heads + h) * HEAD_DIM;
     for (d = 0; d < HEAD_DIM; ++d)
         q[d] = (double)bf16_value(qrow[d]);
@@ -511,7 +512,7 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
     mx = -INFINITY;
     for (j = 0; j < n; ++j) {
         double s = 0.0;
-        if (j >= L && !seen[j - L])
+        if (J->parent != NULL && j >= L && !seen[j - L])
             continue;
         for (d = 0; d < HEAD_DIM; ++d)
             s += q[d] * cache_value(c, 0, row, hk, j, d);
@@ -524,7 +525,7 @@ static int verify_row(verify_job* J, int b, int i, int h, double* o)
     z = 0.0;
     for (j = 0; j < n; ++j) {
         double p;
-        if (j >= L && !seen[j - L])
+        if (J->parent != NULL && j >= L && !seen[j - L])
             continue;
         p = exp(logit[j] - mx);
         z += p;
