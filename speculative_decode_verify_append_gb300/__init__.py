@@ -99,8 +99,9 @@ _lib.spec_accept_sampled.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
-EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn", "verify_attn_noalloc", "spec_accept",
-            "spec_accept_lazy", "spec_accept_tree", "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
+EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn",
+            "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
+            "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
