@@ -63,3 +63,31 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
     args = bench.argparse.Namespace(workload="tiny", steps=1, warmup=3, gpus=2)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_verify_algorithmic_bytes_counts_the_cache_layout():
+    """The roofline's bytes, counted from the oracle's cache arrays: every
+    visible key's K and V codes and the scales that cover it, Q in, O out,
+    the page-table entries used and the lengths."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    import synth
+    for name in ("multi_lane", "int4_12slot", "long_context", "plain_decode", "tiny"):
+        spec = synth.WORKLOADS[name]
+        lens = synth.context_lengths(spec)
+        c = oracle.Cache(spec.kv_dtype, 1, spec.num_kv_heads)  # one page: its arrays give the sizes
+        want = 0
+        for L in lens:
+            n_tok = int(L) + spec.window
+            n_pages = (n_tok + 63) // 64
+            per_token = (c.k_codes.nbytes + c.v_codes.nbytes) // 64
+            if spec.kv_dtype == synth.KV_FP8:  # one scale per page and head
+                want += n_tok * per_token + n_pages * (c.k_scales.nbytes + c.v_scales.nbytes)
+            else:  # scales per token
+                want += n_tok * (per_token + (c.k_scales.nbytes + c.v_scales.nbytes) // 64)
+            want += n_pages * 4 + 4
+        want += 2 * len(lens) * spec.window * spec.num_q_heads * 128 * 2
+        assert bench.verify_algorithmic_bytes(spec, lens) == want, name
