@@ -33,8 +33,9 @@
  *     (NULL = the legacy default stream) and returns.
  *   - Host-side argument errors are returned as negative codes (SDVA_ERR_*)
  *     before anything is enqueued.  Errors that depend on device data (a bad
- *     page id, a lane whose length does not fit, an out-of-vocabulary draft)
- *     are reported by OR-ing SDVA_STATUS_* bits into the optional device int
+ *     page id, a lane whose length does not fit, an out-of-vocabulary draft,
+ *     a per-lane count out of range, a draft tree whose parent is not an
+ *     earlier slot) are reported by OR-ing SDVA_STATUS_* bits into the optional device int
  *     `*status`; the affected lane is skipped as documented per call, never
  *     trapped.  Read `*status` after the stream has completed.
  *   - Launch shapes depend only on host arguments, so every call can be
