@@ -35,9 +35,10 @@
  *     before anything is enqueued.  Errors that depend on device data (a bad
  *     page id, a lane whose length does not fit, an out-of-vocabulary draft,
  *     a per-lane count out of range, a draft tree whose parent is not an
- *     earlier slot) are reported by OR-ing SDVA_STATUS_* bits into the optional device int
- *     `*status`; the affected lane is skipped as documented per call, never
- *     trapped.  Read `*status` after the stream has completed.
+ *     earlier slot) are reported by OR-ing SDVA_STATUS_* bits into the
+ *     optional device int `*status`; the affected lane is skipped as
+ *     documented per call, never trapped.  Read `*status` after the stream
+ *     has completed.
  *   - Launch shapes depend only on host arguments, so every call can be
  *     captured in a CUDA graph and replayed.
  *   - Inputs are not modified except where a parameter says "in/out".
