@@ -159,3 +159,51 @@ def test_header_constants_match_the_binding(lib):
     assert int(defs["SDVA_STATUS_BAD_TREE"]) == sdva.STATUS_BAD_TREE
     assert int(defs["SDVA_STATUS_BAD_DRAFT"]) == sdva.STATUS_BAD_DRAFT
     assert int(defs["SDVA_ERR_WORKSPACE"]) == sdva.ERR_WORKSPACE
+
+
+def test_header_is_plain_c(tmp_path):
+    """sdva.h compiles as C99 with warnings as errors, and every prototype
+    has the type a C caller expects."""
+    src = tmp_path / "use_sdva.c"
+    src.write_text(r'''
+#include "sdva.h"
+typedef int (*append_fn)(const sdva_kv_cache*, const void*, const void*, int, int, const int32_t*, int,
+                         const int32_t*, int32_t*, sdva_stream_t);
+typedef int (*ragged_fn)(const sdva_kv_cache*, const void*, const void*, int, int, const int32_t*,
+                         const int32_t*, int, const int32_t*, int32_t*, sdva_stream_t);
+typedef size_t (*ws_fn)(int, int, int, int, int, int);
+typedef int (*verify_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, int, const int32_t*,
+                         int, float, void*, void*, size_t, int32_t*, sdva_stream_t);
+typedef int (*accept_fn)(const float*, int, int, int, const int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
+                         sdva_stream_t);
+typedef int (*lazy_fn)(const float*, int, int, int, const int32_t*, const int32_t*, int32_t*, int32_t*, int32_t*,
+                       int32_t*, sdva_stream_t);
+typedef int (*tree_fn)(const float*, int, int, int, const int32_t*, const int32_t*, int32_t*, int32_t*, int32_t*,
+                       int32_t*, int32_t*, sdva_stream_t);
+typedef int (*noalloc_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, int, const int32_t*,
+                          int, float, void*, int32_t*, sdva_stream_t);
+typedef size_t (*sws_fn)(int, int);
+typedef int (*sampled_fn)(const float*, const float*, int, int, int, const int32_t*, const float*, const float*,
+                          int32_t*, int32_t*, int32_t*, void*, size_t, int32_t*, sdva_stream_t);
+typedef const char* (*str_fn)(int);
+int check(void) {
+    append_fn a = kv_append_quant;
+    ragged_fn r = kv_append_quant_ragged;
+    ws_fn w = verify_attn_workspace_size;
+    verify_fn v = verify_attn;
+    accept_fn s = spec_accept;
+    lazy_fn l = spec_accept_lazy;
+    tree_fn t = spec_accept_tree;
+    noalloc_fn n = verify_attn_noalloc;
+    sws_fn sw = spec_accept_sampled_workspace_size;
+    sampled_fn sm = spec_accept_sampled;
+    str_fn st = sdva_status_string;
+    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (s != 0) + (l != 0) + (t != 0) + (sw != 0) +
+           (sm != 0) +
+           (st != 0) + SDVA_OK + SDVA_KV_FP8_E4M3 + SDVA_LAZY_WALK_MIN_LANES;
+}
+''')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_sdva.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
