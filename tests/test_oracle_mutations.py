@@ -36,6 +36,17 @@ MUTATIONS = [
      "test_oracle_sampled.py"),
     ("tree rows miss their own key", "            seen[j] = 1;", "            seen[j] = j != i || i == 0;",
      "test_oracle_tree.py"),
+    ("int4 nibbles in the wrong order",
+     "            codes[(g * 32 + i) / 2] = (uint8_t)((q[i] & 0xF) | ((q[i + 1] & 0xF) << 4));",
+     "            codes[(g * 32 + i) / 2] = (uint8_t)((q[i + 1] & 0xF) | ((q[i] & 0xF) << 4));",
+     "test_oracle_append.py"),
+    ("fp8 fresh page keeps the old scale", "    if (start == 0) {", "    if (0) {", "test_oracle_append.py"),
+    ("lazy form ignores the per-lane counts", "        int d = num_drafts ? num_drafts[b] : dmax, a = 0;",
+     "        int d = dmax, a = 0;", "test_oracle_accept.py"),
+    ("residual taken as q - p",
+     "                const double r = p[x] - (double)draft_probs[((size_t)b * d + a) * vocab + x];",
+     "                const double r = (double)draft_probs[((size_t)b * d + a) * vocab + x] - p[x];",
+     "test_oracle_sampled.py"),
 ]
 
 RUNNER = r"""
