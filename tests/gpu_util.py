@@ -70,3 +70,11 @@ def assert_close(got: np.ndarray, want: np.ndarray, what: str = "") -> tuple[flo
                            f"max abs {err.max():.3g}")
     rel = err / np.maximum(np.abs(want), 1e-30)
     return float(err.max()), float(rel.max())
+
+
+def both_fraction(got: np.ndarray, want: np.ndarray) -> float:
+    """Fraction of elements within the stricter reading of the tolerance:
+    |g - r| <= 2e-3 and |g - r| <= 1e-2 |r| at once."""
+    err = np.abs(got.astype(np.float64) - want)
+    ok = (err <= 2e-3) & (err <= 1e-2 * np.abs(want))
+    return float(ok.mean())

@@ -1,15 +1,16 @@
 """GPU parity of verify_attn against the oracle (fp64): every output element
 within |g - r| <= 2e-3 + 1e-2 |r| on small cases spanning several pages,
-splits and ragged tails, FP8 and INT4, and on sampled rows of the five
-full-size workloads in the benchmark's launch configuration; plus GPU-side
-invariants (page-table permutation, split count, invalid lanes)."""
+splits and ragged tails, FP8 and INT4; on the five full-size workloads in
+the benchmark's launch configuration, the KV bytes of two lanes bit for bit,
+every row of one lane and sampled rows of another; plus GPU-side invariants
+(page-table permutation, split count, invalid lanes)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from gpu_util import SM_SCALE, assert_close, bf16_dev, fill_both, i32_dev
+from gpu_util import SM_SCALE, assert_close, bf16_dev, both_fraction, fill_both, i32_dev, lane_pages
 
 pytestmark = pytest.mark.gpu
 
@@ -65,8 +66,27 @@ def test_small_cases_all_elements(case):
     assert_close(got, want, str(case))
 
 
+def _assert_lane_pages_equal(gcache, ocache, step, lanes, what):
+    """Codes and scales of every page the given lanes own, bit for bit."""
+    g = {n: getattr(gcache, n).cpu().numpy() for n in ("k_codes", "v_codes", "k_scales", "v_scales")}
+    for b in lanes:
+        pages = lane_pages(step, b)
+        for n, arr in g.items():
+            got, want = arr[pages], getattr(ocache, n)[pages]
+            got = got.view(np.uint16) if got.dtype == np.float16 else got
+            if got.dtype == np.float32:
+                got, want = got.view(np.uint32), want.view(np.uint32)
+            diff = np.argwhere(got != want)
+            assert diff.size == 0, f"{what} lane {b} {n}: {len(diff)} differing entries, first {diff[:5].tolist()}"
+
+
 @pytest.mark.parametrize("name", ["tiny", "plain_decode", "multi_lane", "long_context", "int4_12slot"])
-def test_full_workload_sampled_rows(name):
+def test_full_workload(name):
+    """At the workload's full size and in the benchmark's launch configuration
+    (max_context = the workload's upper context bound): the KV bytes (codes and
+    scales) of two lanes' pages bit for bit after the context fill and the
+    window append, every row of one lane element by element, and sampled rows
+    of the other lane.  Reports max-abs and max-rel over the compared rows."""
     spec = synth.WORKLOADS[name]
     step = synth.make_step(spec, with_accept=False)
     B, W, Hq = step.q.shape[:3]
@@ -74,18 +94,24 @@ def test_full_workload_sampled_rows(name):
     # the oracle replays the fill of at most two lanes (every lane is on the GPU)
     lanes = sorted(rng.choice(B, size=min(B, 2), replace=False).tolist())
     gcache, ocache, st = fill_both(spec, step, lanes=lanes)
+    assert int(st.item()) == 0
+    _assert_lane_pages_equal(gcache, ocache, step, lanes, name)
     got, status = _run_verify(spec, step, gcache, max_context=spec.ctx_hi)
     assert status == 0
     assert np.isfinite(got).all()
-    rows = []
-    for b in lanes:
+    full = lanes[0]
+    rows = [(full, i, h) for i in range(W) for h in range(Hq)]
+    for b in lanes[1:]:
         for i in sorted({0, W - 1, int(rng.integers(0, W))}):
             for h in sorted({0, Hq - 1, int(rng.integers(0, Hq))}):
                 rows.append((b, i, h))
     want, ost = oracle.verify_attn(ocache, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=rows, threads=16)
     assert ost == 0
     gsel = np.stack([got[b, i, h] for (b, i, h) in rows])
-    assert_close(gsel, want, name)
+    max_abs, max_rel = assert_close(gsel, want, name)
+    # the stricter reading (both bounds at once) is reported, not asserted
+    print(f"{name}: {len(rows)} rows, max abs {max_abs:.3g}, max rel {max_rel:.3g}, "
+          f"both bounds hold for {100.0 * both_fraction(gsel, want):.2f}% of elements")
 
 
 def test_permuted_table_is_bit_identical():
