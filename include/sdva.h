@@ -173,7 +173,8 @@ size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, in
  *   window: 1 .. 16.   max_context: host upper bound on every L_b.
  *   workspace: device scratch of at least verify_attn_workspace_size(...) bytes,
  *     256-byte aligned, used only during the call's kernels (its contents
- *     between calls do not matter).
+ *     between calls do not matter; calls that share a workspace must not
+ *     overlap on the GPU).
  * A lane with L_b < 0, L_b > max_context or L_b + window > 64 *
  * max_pages_per_lane gets SDVA_STATUS_OVERFLOW; a lane with an invalid page id
  * among its first ceil((L_b + window) / 64) entries gets SDVA_STATUS_BAD_PAGE;
@@ -204,9 +205,10 @@ int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int 
  *   Sizes whose verify_attn_workspace_size(...) exceeds
  *   SDVA_NOALLOC_SCRATCH_BYTES are rejected with SDVA_ERR_WORKSPACE before
  *   anything is enqueued.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
- *   capture.
+ *   Every call looks up the array's device address for the device current at
+ *   that call (a host-side query that allocates nothing); the first call on a
+ *   device may also load the library's device code there, so make it before
+ *   any stream capture.
  *   All calls share the one array and it keeps the last call's contents
  *   (nothing in it needs to start at zero): calls whose kernels overlap on the
  *   GPU -- on different streams, or from different threads -- race on it and

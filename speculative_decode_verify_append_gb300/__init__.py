@@ -218,7 +218,7 @@ def verify_attn(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_l
                 max_context: int, sm_scale: float, out: torch.Tensor, workspace: torch.Tensor,
                 status: torch.Tensor | None = None, stream=None) -> None:
     """q, out: bf16 [B][W][Hq][128]; workspace: uint8 device tensor of at least
-    verify_attn_workspace_size(...) bytes."""
+    verify_attn_workspace_size(...) bytes (its contents do not matter)."""
     B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
     s = cache.struct()
     rc = _lib.verify_attn(ctypes.byref(s), _dptr(q, torch.bfloat16, "q"), Hq, B, W,

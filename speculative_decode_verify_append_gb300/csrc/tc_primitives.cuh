@@ -28,19 +28,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
       : "r"(bar), "r"(parity)
       : "memory");
-  return ok != 0;
+  return done != 0;
 }
 
-// As mbar_try_wait, but the thread may sleep in hardware until the phase
-// completes or about `hint_ns` nanoseconds pass, instead of spinning: a
-// waiting warp then takes no issue slots from the warps that do the work.
+// As mbar_test_wait, but the thread may sleep in hardware until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
@@ -53,13 +53,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Wait for the phase with the given parity to complete, giving up after
 // roughly `limit` clock cycles or as soon as *abort becomes non-zero (another
-// role gave up).  Returns false on either.
+// role gave up).  Returns false on either.  kSpin: spin on the non-blocking
+// test, so that a hand-off between two roles is seen a few cycles after it
+// happens; otherwise sleep in mbarrier.try_wait between checks, which leaves
+// the issue slots to the warps that work.  (The FP8 verify kernel measured
+// faster spinning, the INT4 one sleeping.)
+template <bool kSpin>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           long long limit = 4000000000LL) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (kSpin ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 200000u)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) return false;
   }

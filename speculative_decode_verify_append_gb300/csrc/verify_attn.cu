@@ -546,19 +546,17 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   const int threads = plan.warps * 32;
   if (cache->dtype == SDVA_KV_FP8_E4M3) {
     constexpr int smem = split_smem_bytes<SDVA_KV_FP8_E4M3>();
-    static bool attr_done = false;  // per process; the attribute is per function
-    if (!attr_done) {
-      cudaFuncSetAttribute(verify_split_kernel<SDVA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      attr_done = true;
-    }
+    // the shared-memory limit is a per-device attribute of the function: set
+    // it on every call, for the device current now
+    if (cudaFuncSetAttribute(verify_split_kernel<SDVA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return SDVA_ERR_CUDA;
     verify_split_kernel<SDVA_KV_FP8_E4M3><<<grid, threads, smem, s>>>(a);
   } else {
     constexpr int smem = split_smem_bytes<SDVA_KV_INT4_G32>();
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(verify_split_kernel<SDVA_KV_INT4_G32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      attr_done = true;
-    }
+    if (cudaFuncSetAttribute(verify_split_kernel<SDVA_KV_INT4_G32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return SDVA_ERR_CUDA;
     verify_split_kernel<SDVA_KV_INT4_G32><<<grid, threads, smem, s>>>(a);
   }
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
@@ -578,31 +576,19 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
 // SDVA_NOALLOC_SCRATCH_BYTES, and lives on every GPU that loads the library
 // until the process exits.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace sdva {
 namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SDVA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxScratchDevices = 256;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxScratchDevices] = {};  // device address of the array, per device
-
 // Host code must not pass the array's name to a kernel: on the host it is a
-// stand-in symbol, not a device address.  The address is looked up once per
-// device, with that device current, and cached.
+// stand-in symbol, not a device address.  The address is looked up on every
+// call, for the device current at that call (a host-side query, no
+// allocation), so no address outlives the context that produced it.
 int noalloc_scratch_for_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SDVA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxScratchDevices) return SDVA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> guard(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SDVA_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SDVA_ERR_CUDA;
+  *out = p;
   return SDVA_OK;
 }
 

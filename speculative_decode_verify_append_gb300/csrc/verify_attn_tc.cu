@@ -5,12 +5,13 @@
 // and sdva.h): every window row attends over keys 0 .. L_b + i of its kv head.
 //
 // Design (one persistent CTA of 16 warps per SM):
-//   * Work = the flattened list of (lane, kv head, page) triples, cut into
-//     one equal contiguous range per CTA (computed on the device from
-//     seq_lens, so the launch shape depends only on host arguments).  A
-//     maximal run of one (lane, kv head) inside a range is a "segment"; a
-//     segment that is a whole unit writes the final bf16 rows, otherwise it
-//     writes (m, l, O) partials that verify_merge_tc_kernel combines.
+//   * Work = the flattened list of (lane, kv head, page) triples, cut into one
+//     contiguous range per CTA by cost (a unit's pages plus a fixed start cost,
+//     see Partition), computed on the device from seq_lens, so the launch
+//     shape depends only on host arguments.  A maximal run of one (lane, kv
+//     head) inside a range is a "segment"; a segment that is a whole unit
+//     writes the final bf16 rows, otherwise it writes (m, l, O) partials that
+//     verify_merge_tc_kernel combines.
 //   * Pages alternate between two softmax warpgroups by the parity of their
 //     position in the CTA's range.  Each warpgroup has its own S, P and O in
 //     tensor memory and its own running (m, l); at the end of a segment
@@ -21,7 +22,7 @@
 //   * Warps 12-15 (converters): widen each page's V codes to fp16 (exact)
 //     into a second ring, laid out as the MN-major operand of the PV MMA.
 //   * Warps 9-11 issue tcgen05.mma, one thread each:
-//       warp 9 + j: S_j  = Q_hi K^T + Q_lo K^T  (kind::f8f6f4; A = Q from tensor
+//       warp 9 + j: S_j  = Q_hi K^T + Q_lo K^T  (kind::f8f6f4; A = Q from shared
 //                                                memory, B = the page's K tile)
 //       warp 11:    O_j += P_j V                (kind::f16; A = P_j from tensor
 //                                                memory, B = the fp16 V tile)
@@ -291,36 +292,6 @@ __device__ __forceinline__ int q_row_exponent(const uint16_t* qrow) {
   return max(-100, min(100, 8 - k2));
 }
 
-// The Q row scaled by 2^e, split into hi + lo E4M3 codes and stored to row
-// `row` of the two shared-memory operand tiles (128-byte swizzle: 16-byte
-// chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row stores zeros.
-__device__ __forceinline__ void store_q_row_smem(const uint16_t* qrow, int e, uint8_t* qhi, uint8_t* qlo, int row) {
-  const float up = ldexpf(1.0f, e);
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {  // 16 elements per 16-byte chunk
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qrow) v = reinterpret_cast<const uint4*>(qrow)[c * 2 + k];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int t = 0; t < 4; t += 2) {
-        const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
-        const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
-        const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
-        const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
-        const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y), l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
-        hw[2 * k + (t >> 1)] = h01 | (h23 << 16);
-        lw[2 * k + (t >> 1)] = l01 | (l23 << 16);
-      }
-    }
-    const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
-    *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-}
-
 // The Q row scaled by 2^e as fp16, stored to row `row` of the two 64-dim
 // halves of the shared-memory operand (16384 bytes apart; 128-byte swizzle:
 // 8-dim chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row
@@ -337,6 +308,66 @@ __device__ __forceinline__ void store_q16_row_smem(const uint16_t* qrow, int e, 
     for (int t = 0; t < 4; ++t) h[t] = pack_f16x2(bf16_lo(w[t]) * up, bf16_hi(w[t]) * up);
     const uint32_t off = 16384u * (uint32_t)(c >> 3) + (uint32_t)row * 128u + ((uint32_t)((c & 7) ^ (row & 7)) << 4);
     *reinterpret_cast<uint4*>(q + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+// As q_row_exponent, for the FP8 path: the loads go through the
+// non-coherent cache, so that store_q_row_smem re-reads the row from L1.
+__device__ __forceinline__ int q_row_exponent_ldg(const uint16_t* qrow) {
+  if (qrow == nullptr) return 0;
+  uint4 v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = __ldg(reinterpret_cast<const uint4*>(qrow) + k);
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[t])), fabsf(bf16_hi(w[t]))));
+  }
+  if (!(amax > 0.0f)) return 0;
+  int k2;
+  frexpf(amax, &k2);  // amax < 2^k2
+  return max(-100, min(100, 8 - k2));
+}
+
+// The Q row scaled by 2^e, split into hi + lo E4M3 codes and stored to row
+// `row` of the two shared-memory operand tiles (128-byte swizzle: 16-byte
+// chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  A null row stores
+// zeros.  The row is re-read (an L1 hit after q_row_exponent) four chunks at
+// a time, the loads of a group in flight together.
+__device__ __forceinline__ void store_q_row_smem(const uint16_t* qrow, int e, uint8_t* qhi, uint8_t* qlo, int row) {
+  const float up = ldexpf(1.0f, e);
+#pragma unroll 1
+  for (int c0 = 0; c0 < 8; c0 += 4) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      v[k] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow) + c0 * 2 + k) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {  // 16 elements per 16-byte chunk
+      const int c = c0 + cc;
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint4 x = v[cc * 2 + k];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int t = 0; t < 4; t += 2) {
+          const float x0 = bf16_lo(w[t]) * up, x1 = bf16_hi(w[t]) * up;
+          const float x2 = bf16_lo(w[t + 1]) * up, x3 = bf16_hi(w[t + 1]) * up;
+          const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+          const float2 d01 = f32x2_from_e4m3x2(h01), d23 = f32x2_from_e4m3x2(h23);
+          const uint32_t l01 = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y),
+                         l23 = e4m3x2_from_f32(x2 - d23.x, x3 - d23.y);
+          hw[2 * k + (t >> 1)] = h01 | (h23 << 16);
+          lw[2 * k + (t >> 1)] = l01 | (l23 << 16);
+        }
+      }
+      const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
   }
 }
 
@@ -379,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   uint8_t* base_ptr = smem_raw + (base - raw);
   using SM = Smem<KVT>;
   constexpr bool kInt4 = SM::kInt4;
+  constexpr bool kSpinWait = !kInt4;  // see mbar_wait
   constexpr uint32_t kStageBytes = SM::kStageBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(base_ptr + SM::kOffCtl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -400,7 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      // FP8: the copies' expect_tx arrival, then the scale terms; INT4: the
+      // copies' arrival (the scales are inside the stage)
+      mbar_init(smem_u32(&ctl->full[s]), kInt4 ? 1 : 2);
       // FP8: QK commit (K tile), converters (V tile), softmax warps (scales);
       // INT4: converters (K and V codes), softmax warps
       mbar_init(smem_u32(&ctl->empty[s]), (kInt4 ? 0 : 1) + 4 + row_threads / 32);
@@ -469,62 +503,94 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     auto v_scale_of = [&](int ph) -> float {
       return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph & ~kBadPage] : 0.0f);
     };
-    int ph_a = locate(lane), ph_b = locate(32 + lane);
-    float sk_a = k_scale_of(ph_a), sv_a = v_scale_of(ph_a);
     long long issued = 0;
     bool ok = true;
-    for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
-      const int ph_c = locate(g0 + 64 + lane);
-      const float sk_b = k_scale_of(ph_b), sv_b = v_scale_of(ph_b);
-      const float shift_a = sv_a > 0.0f ? log2f(sv_a) : 0.0f;
-      const float inv_a = sv_a > 0.0f ? 1.0f / sv_a : 1.0f;
-      for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
-        const long long g = g0 + i;
-        const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
-        const int ph = ph_m & ~kBadPage;
-        const float sk = __shfl_sync(0xffffffffu, sk_a, i);
-        const float sh = __shfl_sync(0xffffffffu, shift_a, i);
-        const float iv = __shfl_sync(0xffffffffu, inv_a, i);
-        const int s = (int)(g % kStages);
-        if (g >= kStages && !(ok = mbar_wait(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
-          break;
-        if (lane == 0) {
-          const int page_bad = (ph_m & kBadPage) ? 1 : 0;
-          if (page_bad) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
-          ctl->bad[s] = page_bad;
-          ctl->sk[s] = sk;
-          ctl->shift[s] = sh;
-          ctl->inv_v[s] = iv;
-          const uint32_t bar = smem_u32(&ctl->full[s]);
-          const uint32_t dst = stages + s * kStageBytes;
-          mbar_arrive_expect_tx(bar, kStageBytes);
-          if constexpr (kInt4) {
+    if constexpr (kInt4) {
+      // INT4: the scales travel inside the stage (applied by the converters)
+      int ph_a = locate(lane), ph_b = locate(32 + lane);
+      for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
+        const int ph_c = locate(g0 + 64 + lane);
+        for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
+          const long long g = g0 + i;
+          const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
+          const int ph = ph_m & ~kBadPage;
+          const int s = (int)(g % kStages);
+          if (g >= kStages &&
+              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
+            break;
+          if (lane == 0) {
+            const int page_bad = (ph_m & kBadPage) ? 1 : 0;
+            if (page_bad) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
+            ctl->bad[s] = page_bad;
+            ctl->sk[s] = 1.0f;
+            ctl->shift[s] = 0.0f;
+            ctl->inv_v[s] = 1.0f;
+            const uint32_t bar = smem_u32(&ctl->full[s]);
+            const uint32_t dst = stages + s * kStageBytes;
+            mbar_arrive_expect_tx(bar, kStageBytes);
             // K codes | V codes | K scales | V scales, each contiguous per (page, kv head)
             bulk_load(dst, a.k_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
             bulk_load(dst + kI4Codes, a.v_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
-            bulk_load(dst + 2 * kI4Codes, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * kI4Scales, kI4Scales,
-                      bar);
-            bulk_load(dst + 2 * kI4Codes + kI4Scales, static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * kI4Scales,
+            bulk_load(dst + 2 * kI4Codes, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * kI4Scales,
                       kI4Scales, bar);
-          } else {
+            bulk_load(dst + 2 * kI4Codes + kI4Scales,
+                      static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * kI4Scales, kI4Scales, bar);
+          }
+          __syncwarp();
+          issued = g + 1;
+        }
+        ph_a = ph_b;
+        ph_b = ph_c;
+      }
+    } else {
+      // FP8: page ids and scales prefetched 32 pages at a time, two batches ahead
+      int ph_a = locate(lane), ph_b = locate(32 + lane);
+      float sk_a = k_scale_of(ph_a), sv_a = v_scale_of(ph_a);
+      for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
+        const int ph_c = locate(g0 + 64 + lane);
+        const float sk_b = k_scale_of(ph_b), sv_b = v_scale_of(ph_b);
+        for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
+          const long long g = g0 + i;
+          const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
+          const int ph = ph_m & ~kBadPage;
+          const int s = (int)(g % kStages);
+          if (g >= kStages && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
+            break;
+          const uint32_t bar = smem_u32(&ctl->full[s]);
+          if (lane == 0) {
+            // the copies go out as soon as the page id is known; the stage's
+            // scale terms follow with the barrier's second arrival
+            const uint32_t dst = stages + s * kStageBytes;
+            mbar_arrive_expect_tx(bar, kStageBytes);
             tma_load_2d(dst, &map_k, 0, ph * kPage, bar);
             tma_load_2d(dst + kTileBytes, &map_v, 0, ph * kPage, bar);
           }
+          const float sk = __shfl_sync(0xffffffffu, sk_a, i);
+          const float sv = __shfl_sync(0xffffffffu, sv_a, i);
+          if (lane == 0) {
+            const int page_bad = (ph_m & kBadPage) ? 1 : 0;
+            if (page_bad) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
+            ctl->bad[s] = page_bad;
+            ctl->sk[s] = sk;
+            ctl->shift[s] = sv > 0.0f ? log2f(sv) : 0.0f;
+            ctl->inv_v[s] = sv > 0.0f ? 1.0f / sv : 1.0f;
+            mbar_arrive(bar);
+          }
+          __syncwarp();
+          issued = g + 1;
         }
-        __syncwarp();
-        issued = g + 1;
+        ph_a = ph_b;
+        sk_a = sk_b;
+        sv_a = sv_b;
+        ph_b = ph_c;
       }
-      ph_a = ph_b;
-      sk_a = sk_b;
-      sv_a = sv_b;
-      ph_b = ph_c;
     }
     if (!ok) {
       fail(ctl, a.status);
       // drain this CTA's own copies still in flight (bounded)
       for (long long g = max(0LL, issued - kStages); g < issued; ++g) {
         int dummy = 0;
-        mbar_wait(smem_u32(&ctl->full[g % kStages]), (uint32_t)((g / kStages) & 1), &dummy, 400000000LL);
+        mbar_wait<kSpinWait>(smem_u32(&ctl->full[g % kStages]), (uint32_t)((g / kStages) & 1), &dummy, 400000000LL);
       }
     }
   } else if (warp == kQkWarp || warp == kQkWarp + 1) {
@@ -542,18 +608,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     long long g = 0;
     while (g < n_local && ok) {
       const long long seg_len = min((long long)(it.nb - it.p), n_local - g);
-      if (!(ok = mbar_wait(smem_u32(&ctl->q_full), q_phase, abort_flag))) break;
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_full), q_phase, abort_flag))) break;
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
         const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
         // FP8: the page's K tile as loaded; INT4: its fp16 K from the converters
-        if (!(ok = kInt4 ? mbar_wait(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag)
-                         : mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag)))
+        if (!(ok = kInt4 ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag)
+                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag)))
           break;
         const long long n = h >> 1;  // the warpgroup's own page index
         const int x = (int)(n & 1);
         if (n >= 2 &&
-            !(ok = mbar_wait(smem_u32(&ctl->pv_done[j][x]), (uint32_t)(((n >> 1) - 1) & 1), abort_flag)))
+            !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[j][x]), (uint32_t)(((n >> 1) - 1) & 1), abort_flag)))
           break;
         fence_after_sync();
         if (lane == 0) {
@@ -598,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (last >= 0) {
         int dummy = 0;
         const long long n = last >> 1;
-        mbar_wait(smem_u32(&ctl->s_full[j][n & 1]), (uint32_t)((n >> 1) & 1), &dummy, 400000000LL);
+        mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][n & 1]), (uint32_t)((n >> 1) & 1), &dummy, 400000000LL);
       }
     }
   } else if (warp == kPvWarp) {
@@ -619,8 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const long long n = h >> 1;  // the page's index among its warpgroup's pages
         const int x = (int)(n & 1);
         const bool fresh = j ? fresh1 : fresh0;
-        if (!(ok = mbar_wait(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
-        if (!(ok = mbar_wait(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag))) break;
         fence_after_sync();
         if (lane == 0) {
           const uint32_t vt = v16 + t * kV16Bytes;
@@ -645,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       fail(ctl, a.status);
       if (last >= 0) {
         int dummy = 0;
-        mbar_wait(smem_u32(&ctl->v16_empty[last % kV16Stages]), (uint32_t)((last / kV16Stages) & 1), &dummy,
+        mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[last % kV16Stages]), (uint32_t)((last / kV16Stages) & 1), &dummy,
                   400000000LL);
       }
     }
@@ -661,12 +727,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     bool ok = true;
     for (long long h = 0; h < n_local && ok; ++h) {
       const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
-      if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
       if (h >= kV16Stages &&
-          !(ok = mbar_wait(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
         break;
       if (kInt4 && h >= kV16Stages &&
-          !(ok = mbar_wait(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
         break;
       const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
       uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
@@ -748,11 +814,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       const int u = b * a.Hkv + hk;
       const int h = hk * a.G + (row_valid ? row % a.G : 0);
       const uint16_t* qrow = a.q + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
-      const int e = row_valid ? q_row_exponent(qrow) : 0;
+      const int e = kInt4 ? (row_valid ? q_row_exponent(qrow) : 0) : q_row_exponent_ldg(row_valid ? qrow : nullptr);
       if (ok && wg == 0 && warp_active) {
         // the previous segment's QKs are all issued (and, through the
         // segment-end handshake, complete): Q may be overwritten
-        if (seg_count > 0) ok = mbar_wait(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag);
+        if (seg_count > 0) ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag);
         if (ok) {
           // Q into the shared-memory A operand of the QK MMAs
           uint8_t* qb = base_ptr + SM::kOffQ;
@@ -779,9 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const int s = (int)(g % kStages);
         const long long n = g >> 1;  // this warpgroup's own page index
         const int xb = (int)(n & 1);  // its S buffer
-        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
         // the producer staged the page's scale terms before completing full[s]
-        if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
         fence_after_sync();
         const float kscale = ctl->sk[s] * row_scale, shift = ctl->shift[s], inv_f = ctl->inv_v[s];
         seg_bad |= ctl->bad[s];
@@ -819,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (__any_sync(0xffffffffu, need)) {
           // O_j: the PV of the warpgroup's previous page (the latest issued)
           // must have completed
-          if (n >= 1 && !(ok = mbar_wait(smem_u32(&ctl->pv_done[j][xb ^ 1]), (uint32_t)(((n - 1) >> 1) & 1),
+          if (n >= 1 && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[j][xb ^ 1]), (uint32_t)(((n - 1) >> 1) & 1),
                                          abort_flag)))
             break;
           fence_after_sync();
@@ -884,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         long long g_last = g - 1;
         if ((int)(g_last & 1) != wg) --g_last;
         const long long n_last = g_last >> 1;
-        ok = mbar_wait(smem_u32(&ctl->pv_done[wg][n_last & 1]), (uint32_t)((n_last >> 1) & 1), abort_flag);
+        ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[wg][n_last & 1]), (uint32_t)((n_last >> 1) & 1), abort_flag);
         fence_after_sync();
       }
       if (!ok) fail(ctl, a.status);

@@ -26,7 +26,7 @@ def _run_verify(spec, step, gcache, max_context=None, table=None):
     max_context = int(step.seq_lens.max()) if max_context is None else max_context
     table = step.page_table if table is None else table
     out = torch.full((B, W, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(sdva.verify_attn_workspace_size(B, W, Hq, spec.num_kv_heads, max_context), dtype=torch.uint8,
+    ws = torch.zeros(sdva.verify_attn_workspace_size(B, W, Hq, spec.num_kv_heads, max_context), dtype=torch.uint8,
                      device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     sdva.verify_attn(gcache, bf16_dev(step.q), i32_dev(table), i32_dev(step.seq_lens), max_context, float(SM_SCALE),

@@ -37,7 +37,7 @@ def test_noalloc_matches_workspace_call_twice(dtype, lens, W):
     max_context = max(lens)
     q, table, seq = bf16_dev(step.q), i32_dev(step.page_table), i32_dev(step.seq_lens)
 
-    ws = torch.empty(sdva.verify_attn_workspace_size(B, W, Hq, 4, max_context), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(sdva.verify_attn_workspace_size(B, W, Hq, 4, max_context), dtype=torch.uint8, device="cuda")
     ref = torch.empty((B, W, Hq, 128), dtype=torch.bfloat16, device="cuda")
     st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
     sdva.verify_attn(gcache, q, table, seq, max_context, float(SM_SCALE), ref, ws, st_ref)
