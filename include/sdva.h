@@ -17,6 +17,7 @@
  *   kv_append_quant_ragged -- the same with a token count per lane
  *   verify_attn      -- batched, causal-in-window, GQA attention of every
  *                       lane's window over its whole cached context
+ *   verify_attn_tree -- the same for a window that holds a draft tree
  *   spec_accept      -- argmax per window position, longest agreeing draft
  *                       prefix, optional commit of the new lengths
  *   spec_accept_lazy -- the same acceptance reading each lane's rows only up
@@ -185,6 +186,30 @@ int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int 
                 const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens, int max_context,
                 float sm_scale, void* out, void* workspace, size_t workspace_bytes, int32_t* status,
                 sdva_stream_t stream);
+
+/*
+ * verify_attn_tree -- verify_attn for a window that holds a tree of drafted
+ * tokens instead of a chain (MegaCapybara announcement, item 1: drafts and
+ * draft trees).  Reading taken: window slot 0 is the root (the last
+ * committed token) and slot i >= 1 hangs under parent[b][i] < i; the window
+ * is appended in slot order as usual (slot i at position L_b + i).  Row i
+ * attends to the cached context [0, L_b) and to the window keys of its
+ * ancestors and of itself:
+ *     out[b][i][h] = softmax_j(sm_scale * q . K_j) . V_j
+ *                    over j in [0, L_b) and j = L_b + k, k in anc(i) + {i}.
+ * A chain (parent[b][i] = i - 1) gives exactly verify_attn's result.
+ *   parent: int32 [num_lanes][window] (device; entry 0 is not read); may be
+ *           NULL only when window == 1.
+ *   Every other argument, layout and return code is that of verify_attn.
+ * A lane with a parent outside [0, i) gets SDVA_STATUS_BAD_TREE and its
+ * output rows are set to zero (other lanes are unaffected).  Supported up to
+ * 128 rows per kv head (window * num_q_heads / num_kv_heads); larger returns
+ * SDVA_ERR_UNSUPPORTED.
+ */
+int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                     const int32_t* parent, const int32_t* page_table, int max_pages_per_lane,
+                     const int32_t* seq_lens, int max_context, float sm_scale, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t* status, sdva_stream_t stream);
 
 /* Bytes of the fixed device scratch behind verify_attn_noalloc (32 MiB). */
 #define SDVA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -460,10 +460,14 @@ extern "C" size_t verify_attn_workspace_size(int num_lanes, int window, int num_
   return max(plan.bytes, tc::tc_workspace_bytes(num_lanes, window, num_q_heads, num_kv_heads, num_sms));
 }
 
-extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
-                           const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
-                           int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
-                           int32_t* status, sdva_stream_t stream) {
+namespace sdva {
+namespace {
+
+// verify_attn and verify_attn_tree: `parent` null selects the causal window.
+int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                     const int32_t* parent, const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
+                     int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* status, sdva_stream_t stream) {
   if (cache == nullptr || q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr)
     return SDVA_ERR_INVALID;
   // q and out are read and written in 16-byte vectors (and q by bulk copies)
@@ -497,6 +501,7 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
     t.v_codes = static_cast<const uint8_t*>(cache->v_codes);
     t.page_table = page_table;
     t.seq_lens = seq_lens;
+    t.parent = parent;
     t.k_scales = cache->k_scales;
     t.v_scales = cache->v_scales;
     t.ws_ml = reinterpret_cast<float2*>(workspace);
@@ -516,6 +521,8 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
     t.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     return tc::launch_verify_tc(cache, t, num_sms, s);
   }
+  // the mma.sync kernels (more than 128 rows per kv head) know only the causal window
+  if (parent != nullptr) return SDVA_ERR_UNSUPPORTED;
   if (workspace_bytes < plan.bytes) return SDVA_ERR_WORKSPACE;
 
   VerifyArgs a;
@@ -562,6 +569,28 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
   verify_merge_kernel<<<plan.units, 256, 0, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sdva
+
+extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                           const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
+                           int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                           int32_t* status, sdva_stream_t stream) {
+  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, page_table, max_pages_per_lane,
+                                seq_lens, max_context, sm_scale, out, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
+                                int window, const int32_t* parent, const int32_t* page_table, int max_pages_per_lane,
+                                const int32_t* seq_lens, int max_context, float sm_scale, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* status, sdva_stream_t stream) {
+  if (parent == nullptr && window > 1) return SDVA_ERR_INVALID;
+  // a window of one slot is the root alone: the causal kernels
+  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, window > 1 ? parent : nullptr, page_table,
+                                max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
+                                status, stream);
 }
 
 // ---------------------------------------------------------------------------

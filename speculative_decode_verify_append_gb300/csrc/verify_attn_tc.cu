@@ -400,7 +400,7 @@ __device__ __forceinline__ void int4_group_to_f16(uint4 codes, uint32_t scale_bi
   }
 }
 
-template <int KVT>
+template <int KVT, bool kTree>
 __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                     const __grid_constant__ CUtensorMap map_v,
                                                                     TcArgs a) {
@@ -806,6 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     bool ok = true;
     while (g < n_local) {
       // ---- segment setup ----
+      int seg_bad = 0;  // the segment met an out-of-range page id, or the lane's draft tree is invalid
       const int b = it.b, hk = it.hk, nb = it.nb, p0 = it.p;
       const int L = ctl->lens[b];
       const long long g_first = g;
@@ -832,10 +833,33 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       }
       ++seg_count;
       const float row_scale = ldexpf(a.sm_scale_log2, -e);
+      // Draft tree: the window keys L + d this row sees are the set bits d of
+      // `vis` -- its own slot and its ancestors, found by walking the parent
+      // links, held one per lane of the warp (slot k's parent on lane k).  A
+      // parent outside [0, k) makes the lane invalid: its rows are zeroed and
+      // SDVA_STATUS_BAD_TREE is raised.
+      uint32_t vis = 0u;
+      if constexpr (kTree) {
+        const int pk = (lane >= 1 && lane < a.W) ? a.parent[(size_t)b * a.W + lane] : 0;
+        const bool tree_bad = __any_sync(0xffffffffu, lane >= 1 && lane < a.W && (pk < 0 || pk >= lane));
+        int jj = i_row;
+#pragma unroll 1
+        for (int t = 0; t < kMaxWindow; ++t) {
+          vis |= 1u << jj;
+          const int up = __shfl_sync(0xffffffffu, pk, jj);
+          jj = (jj > 0 && !tree_bad) ? up : 0;
+        }
+        if (tree_bad) {
+          seg_bad = 1;
+          if (wg == 0 && row == 0) raise_status(a.status, SDVA_STATUS_BAD_TREE);
+        }
+      }
+      // a row whose visible window keys are slots 0 .. i (a chain) is masked
+      // exactly like the causal window
+      const bool vis_prefix = !kTree || vis == (2u << i_row) - 1u;
 
       float m = -INFINITY, l = 0.0f;
       bool had_page = false;
-      int seg_bad = 0;
       for (long long k = 0; k < seg_len && ok; ++k, ++g) {
         if ((int)(g & 1) != wg) continue;
         had_page = true;
@@ -859,8 +883,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         tmem_ld32(lane_base + col_s(j, xb) + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
         const int kbase = p * kPage;
-        const int lim = L + i_row;  // last visible key position of this row
-        const bool partial = kbase + kPage - 1 > lim;
+        const int lim = L + i_row;  // causal window: last visible key position of this row
+        // a draft tree masks every page that holds window keys key by key:
+        // bit q of vm = key kbase + q is visible (cached context, or a window
+        // key whose bit is set in vis)
+        const int d0 = kbase - L;
+        const bool partial = kbase + kPage - 1 > lim || (!vis_prefix && d0 + kPage - 1 >= 0);
+        uint64_t vm = 0;
+        if (kTree && partial) {
+          const int n_ctx = max(0, -d0);  // < 64 on such a page
+          vm = d0 <= 0 ? (((1ull << n_ctx) - 1ull) | ((uint64_t)vis << n_ctx)) : ((uint64_t)vis >> min(d0, 63));
+        }
         float smax = -INFINITY;
         if (!partial) {
           float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
@@ -875,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         } else {
 #pragma unroll
           for (int q = 0; q < 64; ++q)
-            if (kbase + q <= lim) smax = fmaxf(smax, __uint_as_float(x[q]));
+            if (kTree ? ((vm >> q) & 1ull) != 0 : kbase + q <= lim) smax = fmaxf(smax, __uint_as_float(x[q]));
         }
         const float xmax = smax == -INFINITY ? -INFINITY : fmaf(smax, kscale, shift);
         // The running max may lag the true one by up to kTau (log2 units):
@@ -929,8 +962,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           } else {
 #pragma unroll
             for (int q = 32 * hf; q < 32 * hf + 32; q += 2) {
-              const float w0 = kbase + q <= lim ? fast_exp2(fmaf(__uint_as_float(x[q]), kscale, bias)) : 0.0f;
-              const float w1 = kbase + q + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(x[q + 1]), kscale, bias)) : 0.0f;
+              const bool v0 = kTree ? ((vm >> q) & 1ull) != 0 : kbase + q <= lim;
+              const bool v1 = kTree ? ((vm >> (q + 1)) & 1ull) != 0 : kbase + q + 1 <= lim;
+              const float w0 = v0 ? fast_exp2(fmaf(__uint_as_float(x[q]), kscale, bias)) : 0.0f;
+              const float w1 = v1 ? fast_exp2(fmaf(__uint_as_float(x[q + 1]), kscale, bias)) : 0.0f;
               sum += w0 + w1;
               ph[(q & 31) >> 1] = pack_f16x2(w0, w1);
             }
@@ -1313,19 +1348,19 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
     // the INT4 pools are read with 1-D bulk copies: no tensor maps
     CUtensorMap none;
     memset(&none, 0, sizeof(none));
-    cudaFuncSetAttribute(verify_split_tc_kernel<SDVA_KV_INT4_G32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem_bytes<SDVA_KV_INT4_G32>());
-    verify_split_tc_kernel<SDVA_KV_INT4_G32>
-        <<<num_sms, kThreads, smem_bytes<SDVA_KV_INT4_G32>(), stream>>>(none, none, args);
+    auto kern = args.parent ? verify_split_tc_kernel<SDVA_KV_INT4_G32, true>
+                            : verify_split_tc_kernel<SDVA_KV_INT4_G32, false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_INT4_G32>());
+    kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_INT4_G32>(), stream>>>(none, none, args);
   } else {
     CUtensorMap mk, mv;
     const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
     if (!encode_pool_map(&mk, cache->k_codes, rows) || !encode_pool_map(&mv, cache->v_codes, rows))
       return SDVA_ERR_CUDA;
-    cudaFuncSetAttribute(verify_split_tc_kernel<SDVA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem_bytes<SDVA_KV_FP8_E4M3>());
-    verify_split_tc_kernel<SDVA_KV_FP8_E4M3>
-        <<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
+    auto kern = args.parent ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, true>
+                            : verify_split_tc_kernel<SDVA_KV_FP8_E4M3, false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_FP8_E4M3>());
+    kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
   }
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
   // A unit spans about num_sms / units + 1 CTAs: few -> one warp per row, many

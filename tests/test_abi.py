@@ -159,6 +159,21 @@ def test_header_constants_match_the_binding(lib):
     assert int(defs["SDVA_STATUS_BAD_TREE"]) == sdva.STATUS_BAD_TREE
     assert int(defs["SDVA_STATUS_BAD_DRAFT"]) == sdva.STATUS_BAD_DRAFT
     assert int(defs["SDVA_ERR_WORKSPACE"]) == sdva.ERR_WORKSPACE
+    m = re.search(r"#define SDVA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "SDVA_NOALLOC_SCRATCH_BYTES not found"
+    assert int(m.group(1)) << int(m.group(2)) == sdva.NOALLOC_SCRATCH_BYTES
+
+
+def test_tree_verify_rejects_a_missing_parent_array(lib):
+    """verify_attn_tree validates its arguments on the host: a window of more
+    than one slot needs the parent array."""
+    f = lib.verify_attn_tree
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    fake = ctypes.c_void_p(256)
+    assert f(fake, fake, 24, 2, 4, None, fake, 8, fake, 1000, 0.088, fake, fake, 1 << 20, None, None) == -1
 
 
 def test_header_is_plain_c(tmp_path):
@@ -182,6 +197,8 @@ typedef int (*tree_fn)(const float*, int, int, int, const int32_t*, const int32_
                        int32_t*, int32_t*, sdva_stream_t);
 typedef int (*noalloc_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, int, const int32_t*,
                           int, float, void*, int32_t*, sdva_stream_t);
+typedef int (*tree_verify_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, const int32_t*, int,
+                              const int32_t*, int, float, void*, void*, size_t, int32_t*, sdva_stream_t);
 typedef size_t (*sws_fn)(int, int);
 typedef int (*sampled_fn)(const float*, const float*, int, int, int, const int32_t*, const float*, const float*,
                           int32_t*, int32_t*, int32_t*, void*, size_t, int32_t*, sdva_stream_t);
@@ -195,10 +212,12 @@ int check(void) {
     lazy_fn l = spec_accept_lazy;
     tree_fn t = spec_accept_tree;
     noalloc_fn n = verify_attn_noalloc;
+    tree_verify_fn tv = verify_attn_tree;
     sws_fn sw = spec_accept_sampled_workspace_size;
     sampled_fn sm = spec_accept_sampled;
     str_fn st = sdva_status_string;
-    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (s != 0) + (l != 0) + (t != 0) + (sw != 0) +
+    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (s != 0) + (l != 0) + (t != 0) +
+           (sw != 0) +
            (sm != 0) +
            (st != 0) + SDVA_OK + SDVA_KV_FP8_E4M3 + SDVA_LAZY_WALK_MIN_LANES;
 }
