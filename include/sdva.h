@@ -18,6 +18,7 @@
  *   verify_attn      -- batched, causal-in-window, GQA attention of every
  *                       lane's window over its whole cached context
  *   verify_attn_tree -- the same for a window that holds a draft tree
+ *   verify_attn_ragged -- the same with a window row count per lane
  *   spec_accept      -- argmax per window position, longest agreeing draft
  *                       prefix, optional commit of the new lengths
  *   spec_accept_lazy -- the same acceptance reading each lane's rows only up
@@ -210,6 +211,27 @@ int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int num_q_heads,
                      const int32_t* parent, const int32_t* page_table, int max_pages_per_lane,
                      const int32_t* seq_lens, int max_context, float sm_scale, void* out, void* workspace,
                      size_t workspace_bytes, int32_t* status, sdva_stream_t stream);
+
+/*
+ * verify_attn_ragged -- verify_attn for a padded window whose lanes drafted
+ * different numbers of tokens (the draft count is chosen per workload:
+ * NInfer review, section "아키텍처 ③"), the attention counterpart of
+ * kv_append_quant_ragged.
+ *   n_lane: int32 [num_lanes] (device, required): lane b's window is its
+ *           first n_lane[b] = 1 + d_b rows.  Rows i < n_lane[b] equal
+ *           verify_attn's (they see keys 0 .. L_b + i, all written by the
+ *           ragged append); rows i >= n_lane[b] are written as zeros.
+ * A count outside [0, window] sets SDVA_STATUS_BAD_COUNT and zeroes the
+ * lane's rows.  Every other argument, layout and return code is that of
+ * verify_attn.  Supported up to 128 rows per kv head (window * num_q_heads /
+ * num_kv_heads); larger returns SDVA_ERR_UNSUPPORTED.  The tensor-core tile
+ * holds every window row of a kv head, so the rows past a lane's count cost
+ * no key bytes but still occupy the tile.
+ */
+int verify_attn_ragged(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                       const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
+                       const int32_t* seq_lens, int max_context, float sm_scale, void* out, void* workspace,
+                       size_t workspace_bytes, int32_t* status, sdva_stream_t stream);
 
 /* Bytes of the fixed device scratch behind verify_attn_noalloc (32 MiB). */
 #define SDVA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -251,6 +251,25 @@ def verify_attn(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_le
     return out, int(st[0])
 
 
+def verify_attn_ragged(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
+                       n_lane: np.ndarray, sm_scale: float, threads: int = 1) -> tuple[np.ndarray, int]:
+    """Attention of a padded window with a row count per lane: lane b's rows
+    i < n_lane[b] are verify_attn's rows (keys 0 .. L_b + i), its rows
+    i >= n_lane[b] are zero; a count outside [0, W] zeroes the lane and sets
+    status bit 16 (the per-workload draft count, as in append_ragged)."""
+    q = _as(q_bf16, np.uint16)
+    B, W = q.shape[0], q.shape[1]
+    out, st = verify_attn(cache, q, page_table, seq_lens, sm_scale, threads=threads)
+    for b in range(B):
+        n = int(n_lane[b])
+        if n < 0 or n > W:
+            st |= 16
+            out[b] = 0.0
+        else:
+            out[b, n:] = 0.0
+    return out, st
+
+
 def tree_attn(cache: Cache, q_bf16: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
               parent: np.ndarray, sm_scale: float, threads: int = 1) -> tuple[np.ndarray, int]:
     """fp64 attention of a draft tree's window: row i sees the context and the

@@ -13,6 +13,8 @@ The calls mirror ``include/sdva.h``:
     verify_attn(cache, q, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None, stream=None)
     verify_attn_tree(cache, q, parent, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None,
                      stream=None)
+    verify_attn_ragged(cache, q, n_lane, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None,
+                       stream=None)
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
     spec_accept_lazy(logits, drafts, accept_len, out_tokens, num_drafts=None, seq_lens_inout=None, status=None,
                      stream=None)
@@ -88,6 +90,9 @@ _lib.verify_attn.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P,
 _lib.verify_attn_tree.restype = _I
 _lib.verify_attn_tree.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _P, _I, _P, _I, ctypes.c_float,
                                   _P, _P, ctypes.c_size_t, _P, _P]
+_lib.verify_attn_ragged.restype = _I
+_lib.verify_attn_ragged.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _P, _I, _P, _I, ctypes.c_float,
+                                    _P, _P, ctypes.c_size_t, _P, _P]
 _lib.verify_attn_noalloc.restype = _I
 _lib.verify_attn_noalloc.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float,
                                      _P, _P, _P]
@@ -105,7 +110,7 @@ _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn",
-            "verify_attn_tree", "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
+            "verify_attn_tree", "verify_attn_ragged", "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
             "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -249,6 +254,22 @@ def verify_attn_tree(cache: KVCache, q: torch.Tensor, parent: torch.Tensor | Non
                                workspace.numel() * workspace.element_size(), _dptr(status, torch.int32, "status"),
                                _stream(stream))
     _check("verify_attn_tree", rc)
+
+
+def verify_attn_ragged(cache: KVCache, q: torch.Tensor, n_lane: torch.Tensor, page_table: torch.Tensor,
+                       seq_lens: torch.Tensor, max_context: int, sm_scale: float, out: torch.Tensor,
+                       workspace: torch.Tensor, status: torch.Tensor | None = None, stream=None) -> None:
+    """verify_attn with a window row count per lane: n_lane int32 [B]; rows
+    past a lane's count are written as zeros."""
+    B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+    s = cache.struct()
+    rc = _lib.verify_attn_ragged(ctypes.byref(s), _dptr(q, torch.bfloat16, "q"), Hq, B, W,
+                                 _dptr(n_lane, torch.int32, "n_lane"), _dptr(page_table, torch.int32, "page_table"),
+                                 page_table.shape[1], _dptr(seq_lens, torch.int32, "seq_lens"), int(max_context),
+                                 float(sm_scale), _dptr(out, torch.bfloat16, "out"),
+                                 _dptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+                                 _dptr(status, torch.int32, "status"), _stream(stream))
+    _check("verify_attn_ragged", rc)
 
 
 def verify_attn_noalloc(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,

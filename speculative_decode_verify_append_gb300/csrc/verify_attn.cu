@@ -463,9 +463,11 @@ extern "C" size_t verify_attn_workspace_size(int num_lanes, int window, int num_
 namespace sdva {
 namespace {
 
-// verify_attn and verify_attn_tree: `parent` null selects the causal window.
+// verify_attn, verify_attn_tree and verify_attn_ragged: `parent` null selects
+// the causal window; `n_lane` null, `window` rows for every lane.
 int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
-                     const int32_t* parent, const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
+                     const int32_t* parent, const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
+                     const int32_t* seq_lens,
                      int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
                      int32_t* status, sdva_stream_t stream) {
   if (cache == nullptr || q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr)
@@ -502,6 +504,7 @@ int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads,
     t.page_table = page_table;
     t.seq_lens = seq_lens;
     t.parent = parent;
+    t.n_lane = n_lane;
     t.k_scales = cache->k_scales;
     t.v_scales = cache->v_scales;
     t.ws_ml = reinterpret_cast<float2*>(workspace);
@@ -522,7 +525,7 @@ int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads,
     return tc::launch_verify_tc(cache, t, num_sms, s);
   }
   // the mma.sync kernels (more than 128 rows per kv head) know only the causal window
-  if (parent != nullptr) return SDVA_ERR_UNSUPPORTED;
+  if (parent != nullptr || n_lane != nullptr) return SDVA_ERR_UNSUPPORTED;
   if (workspace_bytes < plan.bytes) return SDVA_ERR_WORKSPACE;
 
   VerifyArgs a;
@@ -578,8 +581,20 @@ extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_
                            const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
                            int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
                            int32_t* status, sdva_stream_t stream) {
-  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, page_table, max_pages_per_lane,
-                                seq_lens, max_context, sm_scale, out, workspace, workspace_bytes, status, stream);
+  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, nullptr, page_table,
+                                max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
+                                status, stream);
+}
+
+extern "C" int verify_attn_ragged(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
+                                  int window, const int32_t* n_lane, const int32_t* page_table,
+                                  int max_pages_per_lane, const int32_t* seq_lens, int max_context, float sm_scale,
+                                  void* out, void* workspace, size_t workspace_bytes, int32_t* status,
+                                  sdva_stream_t stream) {
+  if (n_lane == nullptr) return SDVA_ERR_INVALID;
+  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, n_lane, page_table,
+                                max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
+                                status, stream);
 }
 
 extern "C" int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
@@ -588,7 +603,8 @@ extern "C" int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int n
                                 size_t workspace_bytes, int32_t* status, sdva_stream_t stream) {
   if (parent == nullptr && window > 1) return SDVA_ERR_INVALID;
   // a window of one slot is the root alone: the causal kernels
-  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, window > 1 ? parent : nullptr, page_table,
+  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, window > 1 ? parent : nullptr, nullptr,
+                                page_table,
                                 max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
                                 status, stream);
 }

@@ -400,7 +400,10 @@ __device__ __forceinline__ void int4_group_to_f16(uint4 codes, uint32_t scale_bi
   }
 }
 
-template <int KVT, bool kTree>
+// kMode: bit 0 -- draft-tree window (a.parent); bit 1 -- a window row count
+// per lane (a.n_lane).  Mode 0, the causal window, is the common case.
+constexpr int kModeTree = 1, kModeRagged = 2;
+template <int KVT, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                     const __grid_constant__ CUtensorMap map_v,
                                                                     TcArgs a) {
@@ -410,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   uint8_t* base_ptr = smem_raw + (base - raw);
   using SM = Smem<KVT>;
   constexpr bool kInt4 = SM::kInt4;
+  constexpr bool kTree = (kMode & kModeTree) != 0, kRagged = (kMode & kModeRagged) != 0;
   constexpr bool kSpinWait = !kInt4;  // see mbar_wait
   constexpr uint32_t kStageBytes = SM::kStageBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(base_ptr + SM::kOffCtl);
@@ -857,6 +861,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       // a row whose visible window keys are slots 0 .. i (a chain) is masked
       // exactly like the causal window
       const bool vis_prefix = !kTree || vis == (2u << i_row) - 1u;
+      // per-lane window: rows past the lane's count n_b are written as zeros
+      // (a count outside [0, W] zeroes the lane and raises SDVA_STATUS_BAD_COUNT)
+      bool row_zero = false;
+      if constexpr (kRagged) {
+        const int nb_rows = a.n_lane[b];
+        if (nb_rows < 0 || nb_rows > a.W) {
+          seg_bad = 1;
+          if (wg == 0 && row == 0) raise_status(a.status, SDVA_STATUS_BAD_COUNT);
+        }
+        row_zero = i_row >= nb_rows;
+      }
 
       float m = -INFINITY, l = 0.0f;
       bool had_page = false;
@@ -1009,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       // a page id out of range anywhere in the segment: zero rows for a whole
       // unit, a NaN max marks the partial for the merge
       const bool bad = (seg_bad | ctl->bad1) != 0;
-      if (warp_active && !stop && bad && row_valid) {
+      if (warp_active && !stop && (bad || row_zero) && row_valid) {
         if (whole_unit) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim);
 #pragma unroll 4
@@ -1018,6 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           a.ws_ml[((size_t)(u + c)) * a.R + row] = make_float2(__int_as_float(0x7fc00000), 0.0f);
         }
       }
+      // (warp-uniform: the tensor-memory loads below are warp collectives)
       if (warp_active && !stop && !bad) {
         const float m0 = had0 ? m : -INFINITY, l0 = had0 ? l : 0.0f;
         const float mm1 = ctl->m1[row], ll1 = ctl->l1[row];
@@ -1029,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const float inv = (row_valid && lt > 0.0f) ? 1.0f / (kPScale * lt) : 0.0f;
         uint16_t* orow = nullptr;
         float* prow = nullptr;
-        if (row_valid) {
+        if (row_valid && !row_zero) {
           if (whole_unit)
             orow = a.out + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
           else {
@@ -1348,8 +1364,9 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
     // the INT4 pools are read with 1-D bulk copies: no tensor maps
     CUtensorMap none;
     memset(&none, 0, sizeof(none));
-    auto kern = args.parent ? verify_split_tc_kernel<SDVA_KV_INT4_G32, true>
-                            : verify_split_tc_kernel<SDVA_KV_INT4_G32, false>;
+    auto kern = args.parent   ? verify_split_tc_kernel<SDVA_KV_INT4_G32, kModeTree>
+                : args.n_lane ? verify_split_tc_kernel<SDVA_KV_INT4_G32, kModeRagged>
+                              : verify_split_tc_kernel<SDVA_KV_INT4_G32, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_INT4_G32>());
     kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_INT4_G32>(), stream>>>(none, none, args);
   } else {
@@ -1357,8 +1374,9 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
     const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
     if (!encode_pool_map(&mk, cache->k_codes, rows) || !encode_pool_map(&mv, cache->v_codes, rows))
       return SDVA_ERR_CUDA;
-    auto kern = args.parent ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, true>
-                            : verify_split_tc_kernel<SDVA_KV_FP8_E4M3, false>;
+    auto kern = args.parent   ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, kModeTree>
+                : args.n_lane ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, kModeRagged>
+                              : verify_split_tc_kernel<SDVA_KV_FP8_E4M3, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_FP8_E4M3>());
     kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
   }

@@ -20,6 +20,7 @@ struct TcArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   const int32_t* parent;  // draft tree [B][W] (slot 0 unused) or null for the causal window
+  const int32_t* n_lane;  // window rows per lane (1 + d_b) or null for all `window` rows
   const void* k_scales;  // FP8: f32 [pages][Hkv]; INT4: f16 [pages][Hkv][64][4]
   const void* v_scales;
   float2* ws_ml;  // [lanes * Hkv + ctas][R]

@@ -174,6 +174,9 @@ def test_tree_verify_rejects_a_missing_parent_array(lib):
                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
     fake = ctypes.c_void_p(256)
     assert f(fake, fake, 24, 2, 4, None, fake, 8, fake, 1000, 0.088, fake, fake, 1 << 20, None, None) == -1
+    g = lib.verify_attn_ragged  # the per-lane row counts are required
+    g.restype, g.argtypes = ctypes.c_int, f.argtypes
+    assert g(fake, fake, 24, 2, 4, None, fake, 8, fake, 1000, 0.088, fake, fake, 1 << 20, None, None) == -1
 
 
 def test_header_is_plain_c(tmp_path):
@@ -213,10 +216,12 @@ int check(void) {
     tree_fn t = spec_accept_tree;
     noalloc_fn n = verify_attn_noalloc;
     tree_verify_fn tv = verify_attn_tree;
+    tree_verify_fn rv = verify_attn_ragged;
     sws_fn sw = spec_accept_sampled_workspace_size;
     sampled_fn sm = spec_accept_sampled;
     str_fn st = sdva_status_string;
-    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (s != 0) + (l != 0) + (t != 0) +
+    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (rv != 0) + (s != 0) + (l != 0) +
+           (t != 0) +
            (sw != 0) +
            (sm != 0) +
            (st != 0) + SDVA_OK + SDVA_KV_FP8_E4M3 + SDVA_LAZY_WALK_MIN_LANES;

@@ -59,7 +59,9 @@ def test_multi_step_loop_matches_oracle(dtype):
 def test_ragged_step_loop_matches_oracle(dtype):
     """Lanes with their own draft counts d_b in one padded window: the ragged
     append writes 1 + d_b tokens per lane, verify rows 0 .. d_b are compared,
-    and the lazy acceptance uses the same counts."""
+    verify_attn_ragged gives the same rows bit for bit and zeros past each
+    count (every row against the oracle), and the lazy acceptance uses the
+    same counts."""
     sdva, VerifyStep = _sdva()
     W, Hq, Hkv, V = 8, 12, 2, 3000
     lens = np.array([70, 640, 1333, 5], np.int32)
@@ -90,12 +92,24 @@ def test_ragged_step_loop_matches_oracle(dtype):
         vs.append_ragged(gcache, bf16_dev(stp.k_win), bf16_dev(stp.v_win), i32_dev(d + 1), tdev, L_dev)
         assert oracle.append_ragged(ocache, stp.k_win, stp.v_win, table, L_host, d + 1) == 0
         vs.attend(gcache, bf16_dev(stp.q), tdev, L_dev)
+        q_dev = bf16_dev(stp.q)
+        out_r = torch.full_like(vs.out, float("nan"))
+        sdva.verify_attn_ragged(gcache, q_dev, i32_dev(d + 1), tdev, L_dev, vs.max_context, vs.sm_scale, out_r,
+                                vs.workspace, vs.status)
         vs.accept_lazy(torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts), i32_dev(d), L_dev)
         torch.cuda.synchronize()
         want, _ = oracle.verify_attn(ocache, stp.q, table, L_host, SM_SCALE, threads=8)
         got = vs.out.float().cpu().numpy()
         for b in range(B):  # rows past a lane's count attend to padding: not compared
             assert_close(got[b, :d[b] + 1], want[b, :d[b] + 1], f"step {s} lane {b}")
+        # the ragged verify: every row, the ones past a lane's count zero
+        want_r, st_r = oracle.verify_attn_ragged(ocache, stp.q, table, L_host, d + 1, SM_SCALE, threads=8)
+        assert st_r == 0
+        got_r = out_r.float().cpu().numpy()
+        assert_close(got_r, want_r, f"ragged verify step {s}")
+        for b in range(B):
+            assert not got_r[b, d[b] + 1:].any()
+            assert np.array_equal(got_r[b, :d[b] + 1], got[b, :d[b] + 1])
         acc, tok, newL, _ = oracle.spec_accept_lazy(stp.logits, stp.drafts, d, L_host)
         assert np.array_equal(vs.accept_len.cpu().numpy(), acc)
         assert np.array_equal(vs.out_tokens.cpu().numpy(), tok)

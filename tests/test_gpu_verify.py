@@ -179,3 +179,36 @@ def test_host_argument_errors():
     with pytest.raises(sdva.SdvaError) as e:
         sdva.verify_attn(g2, q3, t, L, 64, 0.088, q3.clone(), ws)
     assert e.value.code == sdva.ERR_INVALID
+
+
+def test_ragged_verify_counts_and_errors():
+    """verify_attn_ragged on a full 8-lane window with counts 0 .. 16 (a lane
+    with 0 rows, a full lane, one count out of range): rows past a count and
+    the rows of the bad lane are zero, SDVA_STATUS_BAD_COUNT is raised, the
+    other rows equal verify_attn bit for bit and the oracle within tolerance."""
+    sdva = _sdva()
+    lens, W = [900, 3000, 64, 5, 12000, 700, 1, 4100], 16
+    spec = synth.Spec("rv", 9, len(lens), 0, 0, 24, 4, W, synth.KV_FP8, None, 0.7, True)
+    step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
+    g, o, _ = fill_both(spec, step, lanes=[0, 1, 5])
+    full, st = _run_verify(spec, step, g)
+    assert st == 0
+    n = np.array([1, 16, 0, 9, 17, 3, 2, 16], np.int32)  # lane 4: out of range
+    B, Hq = len(lens), 24
+    out = torch.full((B, W, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(sdva.verify_attn_workspace_size(B, W, Hq, 4, max(lens)), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sdva.verify_attn_ragged(g, bf16_dev(step.q), i32_dev(n), i32_dev(step.page_table), i32_dev(step.seq_lens),
+                            max(lens), float(SM_SCALE), out, ws, status)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    assert int(status.item()) == sdva.STATUS_BAD_COUNT
+    assert not got[4].any()
+    for b in range(B):
+        if b == 4:
+            continue
+        assert not got[b, n[b]:].any()
+        assert np.array_equal(got[b, :n[b]], full[b, :n[b]])
+    want, _ = oracle.verify_attn_ragged(o, step.q, step.page_table, step.seq_lens, n, SM_SCALE, threads=16)
+    for b in (0, 1, 5):
+        assert_close(got[b], want[b], f"lane {b}")

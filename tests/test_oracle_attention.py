@@ -195,3 +195,29 @@ def test_row_subset_matches_full():
     part, _ = oracle.verify_attn(cache, step.q, step.page_table, step.seq_lens, SM, rows=rows)
     for k, (b, i, h) in enumerate(rows):
         assert np.array_equal(part[k], full[b, i, h])
+
+
+@pytest.mark.parametrize("dtype", [oracle.KV_FP8, oracle.KV_INT4])
+def test_ragged_window_rows(dtype):
+    """Per-lane window row counts: rows i < n_b equal the attention of a
+    window truncated to n_b rows (a separate oracle call with a shorter
+    window) and the torch fp64 softmax; rows past the count are zero; a
+    count outside [0, W] zeroes the lane and sets bit 16."""
+    lens, W, Hq, Hkv = [70, 5, 130], 6, 6, 2
+    spec, step, cache = build(dtype, lens, W, Hq, Hkv, seed=21)
+    n = np.array([0, 4, 6], np.int32)
+    got, st = oracle.verify_attn_ragged(cache, step.q, step.page_table, step.seq_lens, n, SM)
+    assert st == 0
+    want = torch_reference(step, cache)
+    for b in range(len(lens)):
+        assert not got[b, n[b]:].any()
+        assert np.abs(got[b, :n[b]] - want[b, :n[b]]).max(initial=0.0) < 1e-12
+        if n[b]:
+            short, _ = oracle.verify_attn(cache, np.ascontiguousarray(step.q[b:b + 1, :n[b]]),
+                                          step.page_table[b:b + 1], step.seq_lens[b:b + 1], SM)
+            assert np.abs(got[b, :n[b]] - short[0]).max() < 1e-12
+    got2, st2 = oracle.verify_attn_ragged(cache, step.q, step.page_table, step.seq_lens,
+                                          np.array([7, 4, -1], np.int32), SM)
+    assert st2 == 16
+    assert not got2[0].any() and not got2[2].any()
+    assert np.abs(got2[1] - got[1]).max() == 0.0
