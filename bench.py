@@ -7,7 +7,8 @@ table), acceptance over a 151,936-token vocabulary.  Inputs are seeded and
 synthetic and already resident in HBM when the timed region starts.
 
 One JSON line (rank 0):
-  value        verify steps/s (append + verify_attn + spec_accept), device time
+  value        verify steps/s (verify_step: append + verify_attn + spec_accept
+               as one chain of programmatic dependent launches), device time
   verify_attn  achieved algorithmic HBM GB/s of the verify_attn call and its
                fraction of the measured copy bandwidth (roofline object)
   e2e          the same steps/s through the C ABI from pinned HOST buffers,
@@ -19,6 +20,8 @@ One JSON line (rank 0):
                with the step rate it would give
   spec_accept_sampled  lossless stochastic acceptance with a synthetic draft
                distribution (timed apart likewise)
+  all_workloads every workload's verify_attn time, GB/s and fraction of the
+               measured peak, and its step time, measured the same way
   clocks       nvidia-smi SM clocks and throttle reasons during the timed steps
 
 Timing: W untimed warm-up steps, then K steps, each preceded by an untimed L2
@@ -53,10 +56,26 @@ SM_SCALE = np.float32(1.0 / math.sqrt(128.0))
 METRIC = "verify_attn HBM GB/s (% of GB300 peak) and verify steps/s at 8 lanes"
 DEFAULT_WORKLOAD = "multi_lane"
 # dram bytes (read + write) of one verify_attn call (split + merge kernels),
-# measured by ncu for the current kernels, per workload (absent: not captured
-# for this workload, reported as null).  Source: the ncu launch-list summary
-# of the multi-lane workload under profiles/.
-NCU_TRAFFIC_BYTES = {"multi_lane": 305_100_032 + 742_400 + 8_818_432}
+# from an ncu capture of the kernels built from sources with this SHA-256
+# (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order);
+# reported as null once the sources differ (the counters are then stale).
+NCU_TRAFFIC = {"sources_sha256": None, "bytes": {}}
+TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decode_verify_append_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(name: str):
+    if NCU_TRAFFIC["sources_sha256"] != kernel_sources_sha256():
+        return None
+    return NCU_TRAFFIC["bytes"].get(name)
 
 
 def workload_desc(spec: synth.Spec) -> str:
@@ -183,6 +202,37 @@ def max_over_ranks(dist, x: float) -> float:
 
 
 # ---------------------------------------------------------------------------
+# shared by both arms
+# ---------------------------------------------------------------------------
+def bench_config(spec: synth.Spec, seq_lens: np.ndarray, world: int) -> dict:
+    """The `config` object of the JSON line (identical in both arms)."""
+    return {"workload": workload_desc(spec), "lanes": int(len(seq_lens)), "window": spec.window,
+            "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "context_tokens": int(seq_lens.sum()),
+            "parallelism": f"replicas x{world}",
+            "l2": "flushed before every timed step (512 MB write, then 512 MB read of a second buffer; untimed)"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_setup(spec: synth.Spec, step: synth.Step, lanes):
@@ -195,64 +245,78 @@ def oracle_setup(spec: synth.Spec, step: synth.Step, lanes):
     return cache
 
 
-def oracle_sample_step(spec, step, cache, rows, threads):
-    """One bounded sample of a step on the CPU oracle, scaled to a full step.
-    Returns (estimated full-step seconds, sample seconds)."""
+def lane_work(spec: synth.Spec, L: int) -> float:
+    """Attention work of one lane's window (rows x visible keys)."""
+    W = spec.window
+    return W * spec.num_q_heads * (int(L) + (W + 1) / 2)
+
+
+def oracle_lane_step(step: synth.Step, cache, b: int, threads: int) -> float:
+    """One lane's whole verify step on the CPU oracle -- the window append,
+    every window row's attention in fp64, the acceptance -- in seconds.  The
+    append rewrites the same slots with the same values each time."""
     import oracle
     B, W, Hq = step.q.shape[:3]
-    sample_lanes = sorted({r[0] for r in rows})
-    c = cache.copy()
+    sel = slice(b, b + 1)
     t0 = time.perf_counter()
-    sel = np.array(sample_lanes)
-    oracle.append(c, step.k_win[sel], step.v_win[sel], step.page_table[sel], step.seq_lens[sel])
-    t_app = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.verify_attn(c, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=rows, threads=threads)
-    t_att = time.perf_counter() - t0
-    t_acc = 0.0
+    oracle.append(cache, step.k_win[sel], step.v_win[sel], step.page_table[sel], step.seq_lens[sel])
+    rows = [(b, i, h) for i in range(W) for h in range(Hq)]
+    oracle.verify_attn(cache, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=rows, threads=threads)
     if step.logits is not None:
-        t0 = time.perf_counter()
-        oracle.spec_accept(step.logits[sel[:1]], step.drafts[sel[:1]], step.seq_lens[sel[:1]])
-        t_acc = (time.perf_counter() - t0) * B
-    # attention work is proportional to visible keys per row
-    full = sum(W * Hq * (int(L) + (W + 1) / 2) for L in step.seq_lens)
-    part = sum(int(step.seq_lens[b]) + i + 1 for (b, i, h) in rows)
-    est = t_app * B / len(sample_lanes) + t_att * full / part + t_acc
-    return est, t_app + t_att + t_acc / B
+        oracle.spec_accept(step.logits[sel], step.drafts[sel], step.seq_lens[sel])
+    return time.perf_counter() - t0
 
 
-def sample_rows(step, lanes, n, seed):
-    rng = np.random.default_rng(seed)
-    B, W, Hq = step.q.shape[:3]
-    return [(int(rng.choice(lanes)), int(rng.integers(0, W)), int(rng.integers(0, Hq))) for _ in range(n)]
+def oracle_steps(spec, step, cache, lanes, threads, n_steps=None, budget_s=None):
+    """Lane-steps cycling over `lanes` (n_steps of them, or until budget_s has
+    passed and every lane ran once).  Returns (seconds per timed lane-step,
+    full-workload steps per second, lane-steps run)."""
+    times, work = [], 0.0
+    full = sum(lane_work(spec, L) for L in step.seq_lens)
+    t_start = time.perf_counter()
+    k = 0
+    while True:
+        if n_steps is not None and k >= n_steps:
+            break
+        if budget_s is not None and k >= len(lanes) and time.perf_counter() - t_start > budget_s:
+            break
+        b = lanes[k % len(lanes)]
+        times.append(oracle_lane_step(step, cache, b, threads))
+        work += lane_work(spec, step.seq_lens[b])
+        k += 1
+    total = float(np.sum(times))
+    return total / max(1, len(times)), (work / full) / total, len(times)
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores.  Each timed step
+    is one lane of the workload (its window append, all window rows of its
+    attention in fp64, its acceptance), cycling over the lanes; `value`
+    counts the work done in whole-workload steps per second."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     spec = synth.WORKLOADS[args.workload]
     step = synth.make_step(spec)
-    lanes = [0, 1] if spec.num_lanes > 1 else [0]
+    B = len(step.seq_lens)
+    lanes = list(range(B))
     cache = oracle_setup(spec, step, lanes)
     threads = os.cpu_count() or 1
-    ests = []
-    for k in range(args.warmup + args.steps):
-        rows = sample_rows(step, lanes, threads, 1000 + k)
-        est, _ = oracle_sample_step(spec, step, cache, rows, threads)
-        if k >= args.warmup:
-            ests.append(est)
-    sec = float(np.mean(ests))
-    value = 1.0 / sec
+    # warm-up steps on the shortest lane (the oracle is compiled C: nothing to warm but caches)
+    oracle_steps(spec, step, cache, [int(np.argmin(step.seq_lens))], threads, n_steps=args.warmup)
+    sec, value, n = oracle_steps(spec, step, cache, lanes, threads, n_steps=args.steps)
+    model = cpu_model()
+    sample = (f"each timed step: one lane of the {B}-lane workload, cycling over the lanes -- its window append, "
+              f"all {spec.window} x {spec.num_q_heads} attention rows over its whole context in fp64 "
+              f"({threads} threads), its acceptance; value = whole-workload steps/s of the work done")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": workload_desc(spec)},
-        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle",
-                         "sample": f"per step: window append of {len(lanes)} lanes, {threads} attention rows "
-                                   f"(fp64, {threads} threads), acceptance of 1 lane; scaled to the full step by "
-                                   f"visible-key count and lane count"},
+        "config": bench_config(spec, step.seq_lens, world),
+        "step_unit": "one lane per timed step (see cpu_baseline.sample)",
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle", "cpu": model,
+                         "sample": sample},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -262,6 +326,91 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+class GpuWorkload:
+    """One workload resident on the device: the cache filled by the library's
+    own append, the step's inputs, the per-shape buffers."""
+
+    def __init__(self, spec: synth.Spec, dev):
+        import torch
+
+        import speculative_decode_verify_append_gb300 as sdva
+        from speculative_decode_verify_append_gb300.step import VerifyStep, fill_context
+        self.spec = spec
+        self.step = step = synth.make_step(spec)
+        B, W, Hq = step.q.shape[:3]
+        Hkv = spec.num_kv_heads
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.cache = sdva.KVCache(spec.kv_dtype, step.num_pages, Hkv, device=dev)
+        self.table = torch.from_numpy(step.page_table).to(dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        for b in range(B):
+            L = int(step.seq_lens[b])
+            for start, n in synth.fill_chunks(L, 16384):
+                k, v = synth.context_chunk(spec, b, start, n)
+                fill_context(self.cache, bf16(k), bf16(v), self.table[b], start=start, chunk=4096, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        self.seq = torch.from_numpy(step.seq_lens).to(dev)
+        self.commit_lens = self.seq.clone()  # the commit advances a copy: every timed step does the same work
+        self.q, self.kw, self.vw = bf16(step.q), bf16(step.k_win), bf16(step.v_win)
+        self.logits = torch.from_numpy(step.logits).to(dev) if step.logits is not None else None
+        self.drafts = torch.from_numpy(step.drafts).to(dev) if step.drafts is not None else None
+        self.vs = VerifyStep(B, W, Hq, Hkv, spec.ctx_hi, spec.vocab, device=dev)
+        self.alg = verify_algorithmic_bytes(spec, step.seq_lens)
+
+    def separate(self, evs=None):
+        """append, verify_attn, spec_accept as three calls; events between them."""
+        import torch
+        stream = torch.cuda.current_stream()
+        if evs:
+            evs[0].record(stream)
+        self.vs.append(self.cache, self.kw, self.vw, self.table, self.seq)
+        if evs:
+            evs[1].record(stream)
+        self.vs.attend(self.cache, self.q, self.table, self.seq)
+        if evs:
+            evs[2].record(stream)
+        if self.logits is not None:
+            self.vs.accept(self.logits, self.drafts, self.commit_lens)
+        if evs:
+            evs[3].record(stream)
+
+    def reset(self):
+        """Before a chained step (untimed): the step commits into commit_lens,
+        which starts every step at the pre-step lengths, so that every timed
+        step repeats the same work."""
+        self.commit_lens.copy_(self.seq)
+
+    def chained(self):
+        """The whole step in one call (verify_step), or append + verify when the
+        workload has no acceptance."""
+        if self.logits is None:
+            self.separate()
+            return
+        self.vs.step(self.cache, self.q, self.kw, self.vw, self.table, self.commit_lens, self.logits, self.drafts,
+                     commit=True)
+
+    def launches_per_step(self) -> int:
+        return 3 + (2 if self.logits is not None else 0)
+
+
+def time_loop(fn, n_steps, n_warmup, flush_l2, n_events=2):
+    """n_warmup untimed then n_steps timed calls of fn(evs), each after an L2
+    flush; returns the per-step event lists."""
+    import torch
+    for _ in range(n_warmup):
+        flush_l2()
+        fn(None)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(n_steps)]
+    for k in range(n_steps):
+        flush_l2()
+        fn(evs[k])
+    torch.cuda.synchronize()
+    return evs
+
+
 def run_gpu(args):
     import torch
 
@@ -271,33 +420,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
 
     import speculative_decode_verify_append_gb300 as sdva
-    from speculative_decode_verify_append_gb300.step import VerifyStep, fill_context
 
-    spec = synth.WORKLOADS[args.workload]
-    step = synth.make_step(spec)
-    B, W, Hq = step.q.shape[:3]
-    Hkv = spec.num_kv_heads
-    max_context = spec.ctx_hi
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    # ---- resident state: cache filled by the library's own append ----
-    cache = sdva.KVCache(spec.kv_dtype, step.num_pages, Hkv, device=dev)
-    table = torch.from_numpy(step.page_table).to(dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    for b in range(B):
-        L = int(step.seq_lens[b])
-        for start, n in synth.fill_chunks(L, 16384):
-            k, v = synth.context_chunk(spec, b, start, n)
-            fill_context(cache, bf16(k), bf16(v), table[b], start=start, chunk=4096, status=status)
-    torch.cuda.synchronize()
-    seq = torch.from_numpy(step.seq_lens).to(dev)
-    commit_lens = seq.clone()  # the commit advances a copy: the timed steps keep the same work
-    q, kw, vw = bf16(step.q), bf16(step.k_win), bf16(step.v_win)
-    logits = torch.from_numpy(step.logits).to(dev) if step.logits is not None else None
-    drafts = torch.from_numpy(step.drafts).to(dev) if step.drafts is not None else None
-    vs = VerifyStep(B, W, Hq, Hkv, max_context, spec.vocab, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     clean = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
 
@@ -309,23 +432,23 @@ def run_gpu(args):
         clean.amax()
     stream = torch.cuda.current_stream()
 
-    def one_step(evs=None):
+    spec = synth.WORKLOADS[args.workload]
+    wl = GpuWorkload(spec, dev)
+    step, vs = wl.step, wl.vs
+    B, W, Hq = step.q.shape[:3]
+    logits, drafts = wl.logits, wl.drafts
+
+    # ---- the timed steps: verify_step, one call per step ----
+    def chained_step(evs, w=wl):
+        w.reset()
         if evs:
             evs[0].record(stream)
-        vs.append(cache, kw, vw, table, seq)
+        w.chained()
         if evs:
             evs[1].record(stream)
-        vs.attend(cache, q, table, seq)
-        if evs:
-            evs[2].record(stream)
-        if logits is not None:
-            vs.accept(logits, drafts, commit_lens)
-        if evs:
-            evs[3].record(stream)
-
     for _ in range(args.warmup):
         flush_l2()
-        one_step()
+        chained_step(None)
     torch.cuda.synchronize()
     assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
 
@@ -335,7 +458,7 @@ def run_gpu(args):
     except Exception:
         pass
     sampler = ClockSampler(gpu_id)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(dist)
     torch.cuda.synchronize()
     sampler.start()
@@ -344,32 +467,30 @@ def run_gpu(args):
     torch.cuda.nvtx.range_push("timed_steps")
     for k in range(args.steps):
         flush_l2()
-        one_step(evs[k])
+        chained_step(evs[k])
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(dist)
     clocks = sampler.stop()
-    t_app = [e[0].elapsed_time(e[1]) for e in evs]
-    t_att = [e[1].elapsed_time(e[2]) for e in evs]
-    t_acc = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
+    t_step = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = max_over_ranks(dist, float(np.sum(t_step)))
     ms_per_step = total_ms / args.steps
     value = world * args.steps / (total_ms / 1e3)
 
+    # ---- the same step as three calls, timed apart: the per-call breakdown ----
+    sep = time_loop(wl.separate, args.steps, args.warmup, flush_l2, 4)
+    t_app = [e[0].elapsed_time(e[1]) for e in sep]
+    t_att = [e[1].elapsed_time(e[2]) for e in sep]
+    t_acc = [e[2].elapsed_time(e[3]) for e in sep]
+    t_sep = [e[0].elapsed_time(e[3]) for e in sep]
+
     # ---- lazy acceptance (rows read only up to each lane's first disagreement) ----
     lazy = None
     if logits is not None:
-        l_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for k in range(args.warmup + args.steps):
-            flush_l2()
-            if k >= args.warmup:
-                l_ev[k - args.warmup][0].record(stream)
-            vs.accept_lazy(logits, drafts, None, commit_lens)
-            if k >= args.warmup:
-                l_ev[k - args.warmup][1].record(stream)
-        torch.cuda.synchronize()
+        l_ev = time_loop(lambda e: (e and e[0].record(stream), vs.accept_lazy(logits, drafts, None, wl.commit_lens),
+                                    e and e[1].record(stream)), args.steps, args.warmup, flush_l2)
         acc_lazy = vs.accept_len.cpu().numpy().copy()
         tok_lazy = vs.out_tokens.cpu().numpy().copy()
         vs.accept(logits, drafts, None)
@@ -406,15 +527,10 @@ def run_gpu(args):
         ws = torch.empty(sdva.spec_accept_sampled_workspace_size(B, W), dtype=torch.uint8, device=dev)
         s_acc = torch.zeros(B, dtype=torch.int32, device=dev)
         s_tok = torch.zeros((B, W), dtype=torch.int32, device=dev)
-        s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for k in range(args.warmup + args.steps):
-            flush_l2()
-            if k >= args.warmup:
-                s_ev[k - args.warmup][0].record(stream)
-            sdva.spec_accept_sampled(logits, qd, dq, ua, us, s_acc, s_tok, ws, commit_lens, vs.status)
-            if k >= args.warmup:
-                s_ev[k - args.warmup][1].record(stream)
-        torch.cuda.synchronize()
+        s_ev = time_loop(lambda e: (e and e[0].record(stream),
+                                    sdva.spec_accept_sampled(logits, qd, dq, ua, us, s_acc, s_tok, ws, wl.commit_lens,
+                                                             vs.status),
+                                    e and e[1].record(stream)), args.steps, args.warmup, flush_l2)
         assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
         t_s = float(np.mean([e[0].elapsed_time(e[1]) for e in s_ev]))
         a_s = s_acc.cpu().numpy()
@@ -431,6 +547,7 @@ def run_gpu(args):
         del qd
 
     # ---- e2e: host buffers through the public API ----
+    q, kw, vw, seq, table, cache = wl.q, wl.kw, wl.vw, wl.seq, wl.table, wl.cache
     host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("kw", kw), ("vw", vw))}
     if logits is not None:
         host_in["logits"] = logits.cpu().pin_memory()
@@ -472,7 +589,7 @@ def run_gpu(args):
         if logits is not None:
             for ev in logits_ready:
                 stream.wait_event(ev)
-            vs.accept(logits, drafts, commit_lens)
+            vs.accept(logits, drafts, wl.commit_lens)
         host_out["out"].copy_(vs.out, non_blocking=True)
         if logits is not None:
             host_out["acc"].copy_(vs.accept_len, non_blocking=True)
@@ -484,12 +601,32 @@ def run_gpu(args):
     e2e_value = world * e2e_steps / (e2e_ms / 1e3)
 
     # ---- roofline of the verify_attn call ----
-    alg = verify_algorithmic_bytes(spec, step.seq_lens)
+    alg = wl.alg
     att_ms = float(np.mean(t_att))
     achieved = alg / (att_ms / 1e3) / 1e9
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"]
-    traffic = NCU_TRAFFIC_BYTES.get(spec.name)
+    traffic = ncu_traffic(spec.name)
+
+    # ---- every workload, same method: verify_attn alone and the whole step ----
+    all_workloads = None
+    if not args.no_all_workloads:
+        all_workloads = {}
+        for name in synth.WORKLOADS:
+            w = wl if name == spec.name else GpuWorkload(synth.WORKLOADS[name], dev)
+            e_sep = time_loop(w.separate, args.steps, args.warmup, flush_l2, 4)
+            e_ch = time_loop(lambda e: chained_step(e, w), args.steps, args.warmup, flush_l2)
+            assert int(w.vs.status.item()) == 0, (name, sdva.sdva_status_string(int(w.vs.status.item())))
+            v_us = 1e3 * float(np.mean([e[1].elapsed_time(e[2]) for e in e_sep]))
+            st_us = 1e3 * float(np.mean([e[0].elapsed_time(e[1]) for e in e_ch]))
+            sep_us = 1e3 * float(np.mean([e[0].elapsed_time(e[3]) for e in e_sep]))
+            gbs = w.alg / (v_us / 1e6) / 1e9
+            all_workloads[name] = {"verify_attn_us": v_us, "verify_attn_gbs": gbs, "frac": gbs / peak,
+                                   "algorithmic_bytes": w.alg, "step_us": st_us, "steps_per_s": 1e6 / st_us,
+                                   "separate_calls_step_us": sep_us, "kv": "int4" if w.spec.kv_dtype else "fp8"}
+            if w is not wl:
+                del w
+                torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
@@ -497,43 +634,41 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "fp8-e4m3 KV (int4 for the 4-bit workload) -> f16 tensor-core MMA, f32 accumulate, bf16 out",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, N(0,1) fp32 logits)",
-        "config": {"workload": workload_desc(spec), "lanes": B, "window": W, "q_heads": Hq, "kv_heads": Hkv,
-                   "context_tokens": int(step.seq_lens.sum()), "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (512 MB write, then 512 MB read of a second buffer; untimed)"},
+        "config": bench_config(spec, step.seq_lens, world),
+        "step": "verify_step: kv_append_quant + verify_attn + spec_accept as one chain of programmatic dependent "
+                "launches",
         "verify_attn": {"us": att_ms * 1e3, "gbs": achieved, "pct_of_peak": 100.0 * achieved / peak,
                         "algorithmic_bytes": alg},
         "breakdown_us": {"kv_append_quant": float(np.mean(t_app)) * 1e3, "verify_attn": att_ms * 1e3,
-                         "spec_accept": float(np.mean(t_acc)) * 1e3},
+                         "spec_accept": float(np.mean(t_acc)) * 1e3,
+                         "three_separate_calls": float(np.mean(t_sep)) * 1e3,
+                         "verify_step": ms_per_step * 1e3},
         "roofline": {"kernel": "verify_attn (split-K + merge kernels)", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "algorithmic_bytes": alg},
-        "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "calls": "kv_append_quant, verify_attn, spec_accept from pinned host buffers (the logits copy "
+                         "overlaps append and verify)"},
+        "all_workloads": all_workloads,
         "spec_accept_lazy": lazy,
         "spec_accept_sampled": sampled,
-        "gpu_launches": args.steps * (1 + 2 + (2 if logits is not None else 0)),
+        "gpu_launches": args.steps * wl.launches_per_step(),
         "clocks": clocks,
         "wall_s_timed_loop": wall,
     }
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        lanes = [0, 1] if B > 1 else [0]
+        lanes = list(range(B))
         ocache = oracle_setup(spec, step, lanes)
         threads = os.cpu_count() or 1
-        ests = []
-        t_budget = time.perf_counter()
-        k = 0
-        while (k < 3 or time.perf_counter() - t_budget < 10.0) and k < 20:
-            rows = sample_rows(step, lanes, threads, 77 + k)
-            est, _ = oracle_sample_step(spec, step, ocache, rows, threads)
-            ests.append(est)
-            k += 1
+        sec, cvalue, n = oracle_steps(spec, step, ocache, lanes, threads, budget_s=15.0)
         line["cpu_baseline"] = {
-            "value": 1.0 / float(np.mean(ests)), "unit": "steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{k} samples of: window append of {len(lanes)} lanes, {threads} random attention rows "
-                      f"(fp64, {threads} threads), acceptance of 1 lane; scaled to a full step by visible keys "
-                      f"and lanes"}
+            "value": cvalue, "unit": "steps/s", "cores": threads, "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{n} lane-steps cycling over the {B} lanes, each one lane's window append, all "
+                      f"{W} x {Hq} attention rows over its whole context in fp64 ({threads} threads) and its "
+                      f"acceptance; value = whole-workload steps/s of the work done"}
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:
@@ -597,6 +732,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-workloads", action="store_true",
+                    help="skip the all_workloads object (every workload's verify_attn and step times)")
     ap.add_argument("--lazy-sweep", action="store_true",
                     help="time spec_accept vs spec_accept_lazy over lane counts instead of the step")
     args = ap.parse_args(argv)

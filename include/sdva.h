@@ -26,6 +26,8 @@
  *   spec_accept_tree -- greedy acceptance of a tree of drafted tokens
  *   spec_accept_sampled -- lossless stochastic acceptance with the draft
  *                       distribution (ratio test, residual draw)
+ *   verify_step      -- append, verify_attn and spec_accept as one chain of
+ *                       programmatic dependent launches
  *
  * Conventions for every call
  *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA
@@ -264,6 +266,30 @@ int verify_attn_ragged(const sdva_kv_cache* cache, const void* q, int num_q_head
 int verify_attn_noalloc(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
                         const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
                         int max_context, float sm_scale, void* out, int32_t* status, sdva_stream_t stream);
+
+/*
+ * verify_step -- one whole verify step: kv_append_quant (the window's K/V,
+ * n_new = window), verify_attn and spec_accept, on one stream, with results
+ * identical to those three calls made in that order (Baseten talk summary,
+ * section "추측 디코드": the main model checks the drafts in one pass).  The
+ * kernels are chained as programmatic dependent launches, so that each one's
+ * prologue runs while its predecessor drains: the attention's set-up under
+ * the append, the acceptance's argmax beside the attention's merge.
+ *   Arguments: as in the three calls.  k_new, v_new: the window's K/V, bf16
+ *   [num_lanes][window][num_kv_heads][128]; q, out, workspace, max_context,
+ *   sm_scale: as verify_attn; logits, vocab, drafts, accept_len, out_tokens:
+ *   as spec_accept; seq_lens: the pre-step L_b, and with commit != 0 it is
+ *   advanced by 1 + accept_len at the end of the step (in/out).
+ * Preconditions, status bits and return codes are those of the three calls;
+ * the arguments of all three are checked before anything is enqueued (a
+ * call that returns an error enqueues nothing, except that an error from a
+ * CUDA launch may leave earlier kernels of the step enqueued).
+ */
+int verify_step(const sdva_kv_cache* cache, const void* k_new, const void* v_new, const void* q, int num_q_heads,
+                int num_lanes, int window, const int32_t* page_table, int max_pages_per_lane, int32_t* seq_lens,
+                int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                const float* logits, int vocab, const int32_t* drafts, int32_t* accept_len, int32_t* out_tokens,
+                int commit, int32_t* status, sdva_stream_t stream);
 
 /*
  * spec_accept -- greedy acceptance of a verify window.

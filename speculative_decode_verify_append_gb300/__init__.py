@@ -15,6 +15,8 @@ The calls mirror ``include/sdva.h``:
                      stream=None)
     verify_attn_ragged(cache, q, n_lane, page_table, seq_lens, max_context, sm_scale, out, workspace, status=None,
                        stream=None)
+    verify_step(cache, k_new, v_new, q, page_table, seq_lens, max_context, sm_scale, out, workspace, logits, drafts,
+                accept_len, out_tokens, commit=True, status=None, stream=None)
     spec_accept(logits, drafts, accept_len, out_tokens, seq_lens_inout=None, status=None, stream=None)
     spec_accept_lazy(logits, drafts, accept_len, out_tokens, num_drafts=None, seq_lens_inout=None, status=None,
                      stream=None)
@@ -93,6 +95,9 @@ _lib.verify_attn_tree.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I
 _lib.verify_attn_ragged.restype = _I
 _lib.verify_attn_ragged.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _P, _I, _P, _I, ctypes.c_float,
                                     _P, _P, ctypes.c_size_t, _P, _P]
+_lib.verify_step.restype = _I
+_lib.verify_step.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _P, _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float,
+                             _P, _P, ctypes.c_size_t, _P, _I, _P, _P, _P, _I, _P, _P]
 _lib.verify_attn_noalloc.restype = _I
 _lib.verify_attn_noalloc.argtypes = [ctypes.POINTER(_KVCacheStruct), _P, _I, _I, _I, _P, _I, _P, _I, ctypes.c_float,
                                      _P, _P, _P]
@@ -110,7 +115,7 @@ _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn",
-            "verify_attn_tree", "verify_attn_ragged", "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
+            "verify_attn_tree", "verify_attn_ragged", "verify_step", "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
             "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -270,6 +275,28 @@ def verify_attn_ragged(cache: KVCache, q: torch.Tensor, n_lane: torch.Tensor, pa
                                  _dptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
                                  _dptr(status, torch.int32, "status"), _stream(stream))
     _check("verify_attn_ragged", rc)
+
+
+def verify_step(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, page_table: torch.Tensor,
+                seq_lens: torch.Tensor, max_context: int, sm_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                logits: torch.Tensor, drafts: torch.Tensor | None, accept_len: torch.Tensor, out_tokens: torch.Tensor,
+                commit: bool = True, status: torch.Tensor | None = None, stream=None) -> None:
+    """kv_append_quant + verify_attn + spec_accept as one chain of programmatic
+    dependent launches (same results as the three calls in order); with commit,
+    seq_lens is advanced by 1 + accept_len."""
+    B, W, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if logits.dim() != 3 or logits.shape[0] != B or logits.shape[1] != W:
+        raise ValueError("logits must be [B][W][V]")
+    s = cache.struct()
+    rc = _lib.verify_step(ctypes.byref(s), _dptr(k_new, torch.bfloat16, "k_new"), _dptr(v_new, torch.bfloat16, "v_new"),
+                          _dptr(q, torch.bfloat16, "q"), Hq, B, W, _dptr(page_table, torch.int32, "page_table"),
+                          page_table.shape[1], _dptr(seq_lens, torch.int32, "seq_lens"), int(max_context),
+                          float(sm_scale), _dptr(out, torch.bfloat16, "out"), _dptr(workspace, None, "workspace"),
+                          workspace.numel() * workspace.element_size(), _dptr(logits, torch.float32, "logits"),
+                          logits.shape[2], _dptr(drafts, torch.int32, "drafts"),
+                          _dptr(accept_len, torch.int32, "accept_len"), _dptr(out_tokens, torch.int32, "out_tokens"),
+                          1 if commit else 0, _dptr(status, torch.int32, "status"), _stream(stream))
+    _check("verify_step", rc)
 
 
 def verify_attn_noalloc(cache: KVCache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,

@@ -14,6 +14,7 @@
 // intrinsics (__fdiv_rn / __fmul_rn) so that no contraction or approximate
 // division can change a code.
 #include "sdva_common.cuh"
+#include "sdva_internal.cuh"
 
 namespace sdva {
 namespace {
@@ -85,6 +86,9 @@ __device__ __forceinline__ float block_max(float v) {
 
 // grid: (touched-page slot, lane, kv_head * 2 + {0: K, 1: V})
 __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a) {
+  // a kernel launched as this one's programmatic dependent may be scheduled
+  // now; it waits (griddepcontrol.wait) before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int slot = blockIdx.x, b = blockIdx.y;
   const int hk = blockIdx.z >> 1, is_v = blockIdx.z & 1;
   const bool report = slot == 0 && blockIdx.z == 0;
@@ -159,6 +163,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a
 // grid: (touched-page slot, lane).  One thread per (token, kv head, K|V,
 // group of 32 dims): 64 bytes in, 16 bytes of codes and one fp16 scale out.
 __global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs a) {
+  // a kernel launched as this one's programmatic dependent may be scheduled
+  // now; it waits (griddepcontrol.wait) before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int slot = blockIdx.x, b = blockIdx.y;
   const int n = lane_tokens(a, b, slot == 0);
   if (n == 0) return;  // nothing to write: the lane is not examined
@@ -215,10 +222,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs 
 
 using namespace sdva;
 
-namespace {
-int append_impl(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes, int n_new,
-                const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
-                int32_t* status, sdva_stream_t stream) {
+int sdva::append_launch(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes, int n_new,
+                       const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
+                       const int32_t* seq_lens, int32_t* status, sdva_stream_t stream, bool check_only) {
   if (cache == nullptr || k_new == nullptr || v_new == nullptr || page_table == nullptr || seq_lens == nullptr)
     return SDVA_ERR_INVALID;
   if (cache->k_codes == nullptr || cache->v_codes == nullptr || cache->k_scales == nullptr ||
@@ -230,6 +236,7 @@ int append_impl(const sdva_kv_cache* cache, const void* k_new, const void* v_new
   if (cache->page_size != kPage || cache->head_dim != kHeadDim) return SDVA_ERR_UNSUPPORTED;
   if (cache->dtype != SDVA_KV_FP8_E4M3 && cache->dtype != SDVA_KV_INT4_G32) return SDVA_ERR_UNSUPPORTED;
   if (num_lanes > 65535 || cache->num_kv_heads > 32767) return SDVA_ERR_UNSUPPORTED;
+  if (check_only) return SDVA_OK;
   AppendArgs a;
   a.k_new = static_cast<const uint16_t*>(k_new);
   a.v_new = static_cast<const uint16_t*>(v_new);
@@ -254,12 +261,11 @@ int append_impl(const sdva_kv_cache* cache, const void* k_new, const void* v_new
   }
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
 }
-}  // namespace
 
 extern "C" int kv_append_quant(const sdva_kv_cache* cache, const void* k_new, const void* v_new, int num_lanes,
                                int n_new, const int32_t* page_table, int max_pages_per_lane,
                                const int32_t* seq_lens, int32_t* status, sdva_stream_t stream) {
-  return append_impl(cache, k_new, v_new, num_lanes, n_new, nullptr, page_table, max_pages_per_lane, seq_lens,
+  return sdva::append_launch(cache, k_new, v_new, num_lanes, n_new, nullptr, page_table, max_pages_per_lane, seq_lens,
                      status, stream);
 }
 
@@ -268,6 +274,6 @@ extern "C" int kv_append_quant_ragged(const sdva_kv_cache* cache, const void* k_
                                       int max_pages_per_lane, const int32_t* seq_lens, int32_t* status,
                                       sdva_stream_t stream) {
   if (n_lane == nullptr) return SDVA_ERR_INVALID;
-  return append_impl(cache, k_new, v_new, num_lanes, n_new, n_lane, page_table, max_pages_per_lane, seq_lens,
+  return sdva::append_launch(cache, k_new, v_new, num_lanes, n_new, n_lane, page_table, max_pages_per_lane, seq_lens,
                      status, stream);
 }

@@ -36,6 +36,7 @@
 #include <cooperative_groups.h>
 
 #include "sdva_common.cuh"
+#include "sdva_internal.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -145,6 +146,11 @@ __global__ void __launch_bounds__(kArgmaxThreads, 8) argmax_rows_kernel(const fl
     out_tokens[row] = id == 0x7fffffff ? 0 : id;
   }
   cluster.sync();  // rank 0's shared memory must outlive the other CTAs' stores
+  // Launched as a programmatic dependent (verify_step: after verify_attn's
+  // merge), this grid must not finish before that kernel has: the commit of
+  // the finalize kernel, which waits for this grid, rewrites seq_lens, which
+  // the verify kernels read.  A no-op otherwise.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // one warp per lane
@@ -397,7 +403,7 @@ int sm_count(int* sms) {
 }
 // the argmax of every row (num_drafts: of rows 0 .. d_b of every lane)
 int launch_argmax_rows(const float* logits, int num_lanes, int window, int vocab, const int32_t* num_drafts,
-                       int32_t* out_tokens, cudaStream_t s) {
+                       int32_t* out_tokens, cudaStream_t s, bool after_verify = false) {
   const long long rows = (long long)num_lanes * window;
   int sms = 0;
   if (const int rc = sm_count(&sms)) return rc;
@@ -410,13 +416,15 @@ int launch_argmax_rows(const float* logits, int num_lanes, int window, int vocab
   cfg.gridDim = dim3(parts, (unsigned)rows, 1);
   cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = parts;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = after_verify ? 2 : 1;
   const auto kernel = rows_vectorizable(logits, vocab) ? argmax_rows_kernel<true> : argmax_rows_kernel<false>;
   if (cudaLaunchKernelEx(&cfg, kernel, logits, vocab, chunk, num_drafts, window, out_tokens) != cudaSuccess)
     return SDVA_ERR_CUDA;
@@ -438,14 +446,23 @@ int launch_finalize(void (*kernel)(Args...), int num_lanes, cudaStream_t s, Args
 }
 }  // namespace
 
+int sdva::accept_launch(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
+                       int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout, int32_t* status,
+                       sdva_stream_t stream, bool after_verify, bool check_only) {
+  if (const int rc = check_accept_args(logits, num_lanes, window, vocab, drafts, accept_len, out_tokens)) return rc;
+  if (check_only) return SDVA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (const int rc = launch_argmax_rows(logits, num_lanes, window, vocab, nullptr, out_tokens, s, after_verify))
+    return rc;
+  return launch_finalize(accept_finalize_kernel, num_lanes, s, num_lanes, window, vocab, drafts,
+                         (const int32_t*)out_tokens, accept_len, seq_lens_inout, status);
+}
+
 extern "C" int spec_accept(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,
                            int32_t* accept_len, int32_t* out_tokens, int32_t* seq_lens_inout, int32_t* status,
                            sdva_stream_t stream) {
-  if (const int rc = check_accept_args(logits, num_lanes, window, vocab, drafts, accept_len, out_tokens)) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (const int rc = launch_argmax_rows(logits, num_lanes, window, vocab, nullptr, out_tokens, s)) return rc;
-  return launch_finalize(accept_finalize_kernel, num_lanes, s, num_lanes, window, vocab, drafts,
-                         (const int32_t*)out_tokens, accept_len, seq_lens_inout, status);
+  return sdva::accept_launch(logits, num_lanes, window, vocab, drafts, accept_len, out_tokens, seq_lens_inout,
+                             status, stream, false);
 }
 
 extern "C" int spec_accept_lazy(const float* logits, int num_lanes, int window, int vocab, const int32_t* drafts,

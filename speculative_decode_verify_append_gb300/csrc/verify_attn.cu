@@ -25,6 +25,7 @@
 #include <math.h>
 
 #include "sdva_common.cuh"
+#include "sdva_internal.cuh"
 #include "verify_attn_tc.cuh"
 
 namespace sdva {
@@ -461,15 +462,14 @@ extern "C" size_t verify_attn_workspace_size(int num_lanes, int window, int num_
 }
 
 namespace sdva {
-namespace {
 
 // verify_attn, verify_attn_tree and verify_attn_ragged: `parent` null selects
 // the causal window; `n_lane` null, `window` rows for every lane.
-int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
-                     const int32_t* parent, const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
-                     const int32_t* seq_lens,
-                     int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
-                     int32_t* status, sdva_stream_t stream) {
+int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
+                  const int32_t* parent, const int32_t* n_lane, const int32_t* page_table, int max_pages_per_lane,
+                  const int32_t* seq_lens, int max_context, float sm_scale, void* out, void* workspace,
+                  size_t workspace_bytes, int32_t* status, sdva_stream_t stream, bool after_append,
+                  bool check_only) {
   if (cache == nullptr || q == nullptr || page_table == nullptr || seq_lens == nullptr || out == nullptr)
     return SDVA_ERR_INVALID;
   // q and out are read and written in 16-byte vectors (and q by bulk copies)
@@ -496,6 +496,7 @@ int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads,
     // <= 128 rows per kv head: tcgen05 kernels (FP8 or INT4 cache)
     if (workspace_bytes < tc::tc_workspace_bytes(num_lanes, window, num_q_heads, cache->num_kv_heads, num_sms))
       return SDVA_ERR_WORKSPACE;
+    if (check_only) return SDVA_OK;
     const size_t slots = (size_t)num_lanes * cache->num_kv_heads + num_sms;
     tc::TcArgs t;
     t.q = static_cast<const uint16_t*>(q);
@@ -522,11 +523,12 @@ int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads,
     t.max_pages = max_pages_per_lane;
     t.max_context = max_context;
     t.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-    return tc::launch_verify_tc(cache, t, num_sms, s);
+    return tc::launch_verify_tc(cache, t, num_sms, s, after_append);
   }
   // the mma.sync kernels (more than 128 rows per kv head) know only the causal window
   if (parent != nullptr || n_lane != nullptr) return SDVA_ERR_UNSUPPORTED;
   if (workspace_bytes < plan.bytes) return SDVA_ERR_WORKSPACE;
+  if (check_only) return SDVA_OK;
 
   VerifyArgs a;
   a.k_codes = static_cast<const uint8_t*>(cache->k_codes);
@@ -574,16 +576,15 @@ int verify_attn_impl(const sdva_kv_cache* cache, const void* q, int num_q_heads,
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
 }
 
-}  // namespace
 }  // namespace sdva
 
 extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
                            const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,
                            int max_context, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
                            int32_t* status, sdva_stream_t stream) {
-  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, nullptr, page_table,
+  return sdva::verify_launch(cache, q, num_q_heads, num_lanes, window, nullptr, nullptr, page_table,
                                 max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
-                                status, stream);
+                                status, stream, false);
 }
 
 extern "C" int verify_attn_ragged(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
@@ -592,9 +593,9 @@ extern "C" int verify_attn_ragged(const sdva_kv_cache* cache, const void* q, int
                                   void* out, void* workspace, size_t workspace_bytes, int32_t* status,
                                   sdva_stream_t stream) {
   if (n_lane == nullptr) return SDVA_ERR_INVALID;
-  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, nullptr, n_lane, page_table,
+  return sdva::verify_launch(cache, q, num_q_heads, num_lanes, window, nullptr, n_lane, page_table,
                                 max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
-                                status, stream);
+                                status, stream, false);
 }
 
 extern "C" int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes,
@@ -603,10 +604,10 @@ extern "C" int verify_attn_tree(const sdva_kv_cache* cache, const void* q, int n
                                 size_t workspace_bytes, int32_t* status, sdva_stream_t stream) {
   if (parent == nullptr && window > 1) return SDVA_ERR_INVALID;
   // a window of one slot is the root alone: the causal kernels
-  return sdva::verify_attn_impl(cache, q, num_q_heads, num_lanes, window, window > 1 ? parent : nullptr, nullptr,
+  return sdva::verify_launch(cache, q, num_q_heads, num_lanes, window, window > 1 ? parent : nullptr, nullptr,
                                 page_table,
                                 max_pages_per_lane, seq_lens, max_context, sm_scale, out, workspace, workspace_bytes,
-                                status, stream);
+                                status, stream, false);
 }
 
 // ---------------------------------------------------------------------------

@@ -489,6 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       prefetch_tmap(&map_k);
       prefetch_tmap(&map_v);
     }
+    // Launched as a programmatic dependent of the append (verify_step), the
+    // kernel got here while the append may still be writing the cache: wait
+    // for it before the first read of a page or a page scale.  (Q, seq_lens
+    // and the page table are not written by the append.)  A no-op otherwise.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // (page, kv head) index of position g of this CTA's range, -1 past its
     // end; an out-of-range page id loads page 0 instead and is marked with
     // kBadPage (the lane's rows are then written as zeros and flagged)
@@ -1132,6 +1137,9 @@ __device__ __forceinline__ bool merge_locate(const TcArgs& a, int C, int b, int 
 // grid: (units, ceil(R / 8)); block 256 = one warp per row, for units that
 // span few CTAs.  Same duties as verify_merge_tc_kernel below.
 __global__ void __launch_bounds__(256) verify_merge_rows_tc_kernel(TcArgs a, int C) {
+  // a following acceptance launched as a programmatic dependent (verify_step)
+  // may start now: it reads only the logits
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int u = blockIdx.x;
   const int b = u / a.Hkv, hk = u % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1218,6 +1226,9 @@ constexpr int kMergeThreads = 256;
 constexpr int kMaxSegments = 1024;  // >= CTAs of the split kernel (one per SM)
 
 __global__ void __launch_bounds__(kMergeThreads) verify_merge_tc_kernel(TcArgs a, int C) {
+  // a following acceptance launched as a programmatic dependent (verify_step)
+  // may start now: it reads only the logits
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int u = blockIdx.x, r = blockIdx.y;
   const int b = u / a.Hkv, hk = u % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1342,6 +1353,24 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows) {
 
 }  // namespace
 
+// The split kernel, one CTA per SM; with after_append, as a programmatic
+// dependent of the kernel before it on the stream (the append of verify_step).
+cudaError_t launch_split(void (*kern)(CUtensorMap, CUtensorMap, TcArgs), const CUtensorMap& mk,
+                         const CUtensorMap& mv, const TcArgs& args, int num_sms, size_t smem, cudaStream_t stream,
+                         bool after_append) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_append ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
+}
+
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms) {
   const int R = W * (Hq / Hkv);
   const size_t slots = (size_t)B * Hkv + (size_t)num_sms;
@@ -1359,7 +1388,8 @@ bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_page
          (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }
 
-int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream) {
+int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream,
+                     bool after_append) {
   if (cache->dtype == SDVA_KV_INT4_G32) {
     // the INT4 pools are read with 1-D bulk copies: no tensor maps
     CUtensorMap none;
@@ -1368,7 +1398,9 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
                 : args.n_lane ? verify_split_tc_kernel<SDVA_KV_INT4_G32, kModeRagged>
                               : verify_split_tc_kernel<SDVA_KV_INT4_G32, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_INT4_G32>());
-    kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_INT4_G32>(), stream>>>(none, none, args);
+    if (launch_split(kern, none, none, args, num_sms, smem_bytes<SDVA_KV_INT4_G32>(), stream, after_append) !=
+        cudaSuccess)
+      return SDVA_ERR_CUDA;
   } else {
     CUtensorMap mk, mv;
     const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
@@ -1378,7 +1410,9 @@ int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
                 : args.n_lane ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, kModeRagged>
                               : verify_split_tc_kernel<SDVA_KV_FP8_E4M3, 0>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_FP8_E4M3>());
-    kern<<<num_sms, kThreads, smem_bytes<SDVA_KV_FP8_E4M3>(), stream>>>(mk, mv, args);
+    if (launch_split(kern, mk, mv, args, num_sms, smem_bytes<SDVA_KV_FP8_E4M3>(), stream, after_append) !=
+        cudaSuccess)
+      return SDVA_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
   // A unit spans about num_sms / units + 1 CTAs: few -> one warp per row, many

@@ -35,8 +35,11 @@ struct TcArgs {
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms);
 // Whether the tcgen05 path handles this call (<= 128 rows per kv head, ...).
 bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_pages, int num_sms);
-// Enqueue the split and merge kernels on `stream`.
-int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream);
+// Enqueue the split and merge kernels on `stream`; with after_append the split
+// kernel is a programmatic dependent of the kernel enqueued just before it,
+// which must write nothing but the cache (verify_step's append).
+int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream,
+                     bool after_append);
 
 }  // namespace tc
 }  // namespace sdva

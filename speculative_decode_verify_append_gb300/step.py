@@ -13,7 +13,7 @@ import math
 import torch
 
 from . import (KVCache, kv_append_quant, kv_append_quant_ragged, spec_accept, spec_accept_lazy, verify_attn,
-               verify_attn_workspace_size)
+               verify_attn_workspace_size, verify_step)
 
 
 class VerifyStep:
@@ -49,6 +49,13 @@ class VerifyStep:
         """Acceptance reading each lane's rows only up to its first disagreement."""
         spec_accept_lazy(logits, drafts, self.accept_len, self.out_tokens, num_drafts, seq_lens_inout, self.status,
                          stream)
+
+    def step(self, cache: KVCache, q, k_win, v_win, page_table, seq_lens, logits, drafts, commit: bool = True,
+             stream=None):
+        """The whole step in one library call (verify_step): the same results
+        as run(), the three calls chained as programmatic dependent launches."""
+        verify_step(cache, k_win, v_win, q, page_table, seq_lens, self.max_context, self.sm_scale, self.out,
+                    self.workspace, logits, drafts, self.accept_len, self.out_tokens, commit, self.status, stream)
 
     def run(self, cache: KVCache, q, k_win, v_win, page_table, seq_lens, logits=None, drafts=None,
             commit: bool = True, stream=None):

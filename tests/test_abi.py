@@ -200,6 +200,9 @@ typedef int (*tree_fn)(const float*, int, int, int, const int32_t*, const int32_
                        int32_t*, int32_t*, sdva_stream_t);
 typedef int (*noalloc_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, int, const int32_t*,
                           int, float, void*, int32_t*, sdva_stream_t);
+typedef int (*step_fn)(const sdva_kv_cache*, const void*, const void*, const void*, int, int, int, const int32_t*, int,
+                       int32_t*, int, float, void*, void*, size_t, const float*, int, const int32_t*, int32_t*,
+                       int32_t*, int, int32_t*, sdva_stream_t);
 typedef int (*tree_verify_fn)(const sdva_kv_cache*, const void*, int, int, int, const int32_t*, const int32_t*, int,
                               const int32_t*, int, float, void*, void*, size_t, int32_t*, sdva_stream_t);
 typedef size_t (*sws_fn)(int, int);
@@ -217,10 +220,11 @@ int check(void) {
     noalloc_fn n = verify_attn_noalloc;
     tree_verify_fn tv = verify_attn_tree;
     tree_verify_fn rv = verify_attn_ragged;
+    step_fn vs = verify_step;
     sws_fn sw = spec_accept_sampled_workspace_size;
     sampled_fn sm = spec_accept_sampled;
     str_fn st = sdva_status_string;
-    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (rv != 0) + (s != 0) + (l != 0) +
+    return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (rv != 0) + (vs != 0) + (s != 0) + (l != 0) +
            (t != 0) +
            (sw != 0) +
            (sm != 0) +

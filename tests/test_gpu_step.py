@@ -180,3 +180,76 @@ def test_checkpoint_restore_continues_identically():
     second = [one_step("b"), one_step("c")]
     for (o1, a1), (o2, a2) in zip(first, second):
         assert torch.equal(o1, o2) and torch.equal(a1, a2)
+
+
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+def test_verify_step_equals_the_three_calls(dtype):
+    """verify_step (the chained launch) leaves the same cache bytes, attention
+    rows, accept lengths, tokens, committed lengths and status as
+    kv_append_quant, verify_attn and spec_accept called in order -- bit for
+    bit -- over three steps, with and without the commit."""
+    sdva, VerifyStep = _sdva()
+    W, Hq, Hkv, V = 16 if dtype == synth.KV_FP8 else 8, 24, 4, 151936
+    lens = np.array([4096, 700, 9000, 64, 33000, 5], np.int32)
+    B = len(lens)
+    spec = synth.Spec("chain", 14 + dtype, B, 0, 0, Hq, Hkv, W, dtype, V, 0.7, True)
+    table, total = synth.page_table_for(spec, lens + 3 * W, W)
+    caches = []
+    for _ in range(2):
+        g = sdva.KVCache(dtype, total, Hkv)
+        tdev = i32_dev(table)
+        for b, L in enumerate(lens):
+            for start, n in synth.fill_chunks(int(L), 4096):
+                k, v = synth.context_chunk(spec, b, start, n)
+                sdva.kv_append_quant(g, bf16_dev(k[None]), bf16_dev(v[None]), tdev[b:b + 1],
+                                     i32_dev(np.array([start])))
+        caches.append(g)
+    va, vb = (VerifyStep(B, W, Hq, Hkv, int(lens.max()) + 3 * W, V) for _ in range(2))
+    La, Lb = i32_dev(lens), i32_dev(lens)
+    tdev = i32_dev(table)
+    L_host = lens.copy()
+    for s in range(3):
+        stp = synth.make_step(spec, seq_lens=L_host, tag=f"c{s}")
+        q, kw, vw = bf16_dev(stp.q), bf16_dev(stp.k_win), bf16_dev(stp.v_win)
+        lg, dr = torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts)
+        commit = s != 1
+        va.run(caches[0], q, kw, vw, tdev, La, lg, dr, commit=commit)
+        vb.step(caches[1], q, kw, vw, tdev, Lb, lg, dr, commit=commit)
+        torch.cuda.synchronize()
+        for x, y, name in ((va.out, vb.out, "out"), (va.accept_len, vb.accept_len, "accept_len"),
+                           (va.out_tokens, vb.out_tokens, "out_tokens"), (La, Lb, "seq_lens"),
+                           (va.status, vb.status, "status")):
+            assert torch.equal(x, y), (s, name)
+        L_host = La.cpu().numpy()
+    assert int(va.status.item()) == 0
+    for n in ("k_codes", "v_codes", "k_scales", "v_scales"):
+        assert torch.equal(getattr(caches[0], n), getattr(caches[1], n)), n
+
+
+def test_verify_step_in_a_cuda_graph():
+    """verify_step captures and replays in a CUDA graph with the eager results."""
+    sdva, VerifyStep = _sdva()
+    lens = np.array([4096, 700, 9000, 64], np.int32)
+    spec = synth.Spec("g2", 3, 4, 0, 0, 24, 4, 16, synth.KV_FP8, 151936, 0.7, True)
+    stp = synth.make_step(spec, seq_lens=lens)
+    gcache, _, _ = fill_both(spec, stp, with_oracle=False)
+    vs = VerifyStep(4, 16, 24, 4, 9000, 151936)
+    q, t, L = bf16_dev(stp.q), i32_dev(stp.page_table), i32_dev(lens)
+    lg, dr = torch.from_numpy(stp.logits).cuda(), i32_dev(stp.drafts)
+    kw, vw = bf16_dev(stp.k_win), bf16_dev(stp.v_win)
+    vs.step(gcache, q, kw, vw, t, L, lg, dr, commit=False)
+    torch.cuda.synchronize()
+    eager = (vs.out.clone(), vs.accept_len.clone(), vs.out_tokens.clone())
+    vs.out.zero_()
+    vs.accept_len.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            vs.step(gcache, q, kw, vw, t, L, lg, dr, commit=False, stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(vs.out, eager[0]) and torch.equal(vs.accept_len, eager[1])
+    assert torch.equal(vs.out_tokens, eager[2])
+    assert int(vs.status.item()) == 0
