@@ -413,6 +413,19 @@ int spec_accept_sampled(const float* logits, const float* draft_probs, int num_l
                         int32_t* out_tokens, int32_t* seq_lens_inout, void* workspace, size_t workspace_bytes,
                         int32_t* status, sdva_stream_t stream);
 
+/*
+ * sdva_debug_set_wait_limit -- diagnostic hook (no counterpart in the pages).
+ * Every device-side wait of verify_attn's tensor-core kernels gives up after
+ * `cycles` clock cycles (default about 4e9, two seconds); the CTA then
+ * raises SDVA_STATUS_TIMEOUT, waits (with its own bound) for the copies and
+ * tensor-core work it issued, frees its tensor memory and returns, leaving
+ * the context usable (the output of such a call is undefined).  A negative
+ * value restores the default.  Returns the previous limit.  Applies to
+ * calls enqueued after it returns; not synchronised with concurrent calls.
+ * Meant for tests that make a wait run out.
+ */
+long long sdva_debug_set_wait_limit(long long cycles);
+
 /* Static description of a return code or status bit set (never NULL). */
 const char* sdva_status_string(int code);
 

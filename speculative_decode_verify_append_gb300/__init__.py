@@ -111,12 +111,15 @@ _lib.spec_accept_sampled_workspace_size.restype = ctypes.c_size_t
 _lib.spec_accept_sampled_workspace_size.argtypes = [_I, _I]
 _lib.spec_accept_sampled.restype = _I
 _lib.spec_accept_sampled.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+_lib.sdva_debug_set_wait_limit.restype = ctypes.c_longlong
+_lib.sdva_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
 _lib.sdva_status_string.restype = ctypes.c_char_p
 _lib.sdva_status_string.argtypes = [_I]
 
 EXPORTED = ("kv_append_quant", "kv_append_quant_ragged", "verify_attn_workspace_size", "verify_attn",
             "verify_attn_tree", "verify_attn_ragged", "verify_step", "verify_attn_noalloc", "spec_accept", "spec_accept_lazy", "spec_accept_tree",
-            "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_status_string")
+            "spec_accept_sampled_workspace_size", "spec_accept_sampled", "sdva_debug_set_wait_limit",
+            "sdva_status_string")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -124,6 +127,13 @@ class SdvaError(RuntimeError):
     def __init__(self, call: str, code: int):
         super().__init__(f"{call}: {sdva_status_string(code)} (code {code})")
         self.code = code
+
+
+def sdva_debug_set_wait_limit(cycles: int) -> int:
+    """Bound every device wait of verify_attn's tensor-core kernels at `cycles`
+    clock cycles (negative: the default, about two seconds); returns the
+    previous bound.  A wait that runs out raises STATUS_TIMEOUT."""
+    return int(_lib.sdva_debug_set_wait_limit(int(cycles)))
 
 
 def sdva_status_string(code: int) -> str:

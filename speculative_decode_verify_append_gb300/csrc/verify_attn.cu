@@ -24,6 +24,8 @@
 //     kernel merges them by log-sum-exp and writes bf16 rows.
 #include <math.h>
 
+#include <atomic>
+
 #include "sdva_common.cuh"
 #include "sdva_internal.cuh"
 #include "verify_attn_tc.cuh"
@@ -463,6 +465,9 @@ extern "C" size_t verify_attn_workspace_size(int num_lanes, int window, int num_
 
 namespace sdva {
 
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // clock cycles, about two seconds
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
 // verify_attn, verify_attn_tree and verify_attn_ragged: `parent` null selects
 // the causal window; `n_lane` null, `window` rows for every lane.
 int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
@@ -523,6 +528,7 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
     t.max_pages = max_pages_per_lane;
     t.max_context = max_context;
     t.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    t.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     return tc::launch_verify_tc(cache, t, num_sms, s, after_append);
   }
   // the mma.sync kernels (more than 128 rows per kv head) know only the causal window
@@ -577,6 +583,10 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
 }
 
 }  // namespace sdva
+
+extern "C" long long sdva_debug_set_wait_limit(long long cycles) {
+  return sdva::g_wait_limit.exchange(cycles < 0 ? sdva::kDefaultWaitLimit : cycles);
+}
 
 extern "C" int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
                            const int32_t* page_table, int max_pages_per_lane, const int32_t* seq_lens,

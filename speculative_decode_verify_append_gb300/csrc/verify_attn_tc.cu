@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           const int ph = ph_m & ~kBadPage;
           const int s = (int)(g % kStages);
           if (g >= kStages &&
-              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
+              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag, a.wait_limit)))
             break;
           if (lane == 0) {
             const int page_bad = (ph_m & kBadPage) ? 1 : 0;
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
           const int ph = ph_m & ~kBadPage;
           const int s = (int)(g % kStages);
-          if (g >= kStages && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag)))
+          if (g >= kStages && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag, a.wait_limit)))
             break;
           const uint32_t bar = smem_u32(&ctl->full[s]);
           if (lane == 0) {
@@ -617,18 +617,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     long long g = 0;
     while (g < n_local && ok) {
       const long long seg_len = min((long long)(it.nb - it.p), n_local - g);
-      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_full), q_phase, abort_flag))) break;
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_full), q_phase, abort_flag, a.wait_limit))) break;
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
         const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
         // FP8: the page's K tile as loaded; INT4: its fp16 K from the converters
-        if (!(ok = kInt4 ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag)
-                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag)))
+        if (!(ok = kInt4 ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit)
+                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag, a.wait_limit)))
           break;
         const long long n = h >> 1;  // the warpgroup's own page index
         const int x = (int)(n & 1);
         if (n >= 2 &&
-            !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[j][x]), (uint32_t)(((n >> 1) - 1) & 1), abort_flag)))
+            !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[j][x]), (uint32_t)(((n >> 1) - 1) & 1), abort_flag, a.wait_limit)))
           break;
         fence_after_sync();
         if (lane == 0) {
@@ -694,8 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const long long n = h >> 1;  // the page's index among its warpgroup's pages
         const int x = (int)(n & 1);
         const bool fresh = j ? fresh1 : fresh0;
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag, a.wait_limit))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit))) break;
         fence_after_sync();
         if (lane == 0) {
           const uint32_t vt = v16 + t * kV16Bytes;
@@ -736,12 +736,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     bool ok = true;
     for (long long h = 0; h < n_local && ok; ++h) {
       const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
-      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag))) break;
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag, a.wait_limit))) break;
       if (h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
       if (kInt4 && h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
       const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
       uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (ok && wg == 0 && warp_active) {
         // the previous segment's QKs are all issued (and, through the
         // segment-end handshake, complete): Q may be overwritten
-        if (seg_count > 0) ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag);
+        if (seg_count > 0) ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_free), (seg_count - 1) & 1u, abort_flag, a.wait_limit);
         if (ok) {
           // Q into the shared-memory A operand of the QK MMAs
           uint8_t* qb = base_ptr + SM::kOffQ;
@@ -889,9 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         const int s = (int)(g % kStages);
         const long long n = g >> 1;  // this warpgroup's own page index
         const int xb = (int)(n & 1);  // its S buffer
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag, a.wait_limit))) break;
         // the producer staged the page's scale terms before completing full[s]
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag, a.wait_limit))) break;
         fence_after_sync();
         const float kscale = ctl->sk[s] * row_scale, shift = ctl->shift[s], inv_f = ctl->inv_v[s];
         seg_bad |= ctl->bad[s];
@@ -939,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           // O_j: the PV of the warpgroup's previous page (the latest issued)
           // must have completed
           if (n >= 1 && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[j][xb ^ 1]), (uint32_t)(((n - 1) >> 1) & 1),
-                                         abort_flag)))
+                                         abort_flag, a.wait_limit)))
             break;
           fence_after_sync();
           const float m_new = m == -INFINITY ? m : fmaxf(m, xmax);
@@ -1005,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         long long g_last = g - 1;
         if ((int)(g_last & 1) != wg) --g_last;
         const long long n_last = g_last >> 1;
-        ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[wg][n_last & 1]), (uint32_t)((n_last >> 1) & 1), abort_flag);
+        ok = mbar_wait<kSpinWait>(smem_u32(&ctl->pv_done[wg][n_last & 1]), (uint32_t)((n_last >> 1) & 1), abort_flag, a.wait_limit);
         fence_after_sync();
       }
       if (!ok) fail(ctl, a.status);

@@ -28,6 +28,7 @@ struct TcArgs {
   uint16_t* out;  // bf16 [B][W][Hq][128]
   int32_t* status;
   int num_pages, B, Hkv, Hq, G, W, R, max_pages, max_context;
+  long long wait_limit;  // clock cycles a device wait may take before the CTA gives up
   float sm_scale_log2;
 };
 

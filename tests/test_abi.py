@@ -209,6 +209,7 @@ typedef size_t (*sws_fn)(int, int);
 typedef int (*sampled_fn)(const float*, const float*, int, int, int, const int32_t*, const float*, const float*,
                           int32_t*, int32_t*, int32_t*, void*, size_t, int32_t*, sdva_stream_t);
 typedef const char* (*str_fn)(int);
+typedef long long (*limit_fn)(long long);
 int check(void) {
     append_fn a = kv_append_quant;
     ragged_fn r = kv_append_quant_ragged;
@@ -224,11 +225,12 @@ int check(void) {
     sws_fn sw = spec_accept_sampled_workspace_size;
     sampled_fn sm = spec_accept_sampled;
     str_fn st = sdva_status_string;
+    limit_fn lim = sdva_debug_set_wait_limit;
     return (a != 0) + (r != 0) + (w != 0) + (v != 0) + (n != 0) + (tv != 0) + (rv != 0) + (vs != 0) + (s != 0) + (l != 0) +
            (t != 0) +
            (sw != 0) +
            (sm != 0) +
-           (st != 0) + SDVA_OK + SDVA_KV_FP8_E4M3 + SDVA_LAZY_WALK_MIN_LANES;
+           (st != 0) + (lim != 0) + SDVA_OK + SDVA_KV_FP8_E4M3 + SDVA_LAZY_WALK_MIN_LANES;
 }
 ''')
     r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",

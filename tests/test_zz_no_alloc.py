@@ -6,9 +6,11 @@ hands over only the operator's own tensors, or a latency-critical loop that
 cannot afford an allocator's implicit synchronisation.  verify_attn_noalloc
 serves them by taking its split-K scratch from a fixed array inside the
 library.  These tests call it through the C ABI (the ctypes binding) and
-check it against verify_attn with a caller workspace, on two calls in a row,
-within the tolerance the parity tests use; and check that sizes whose scratch
-would not fit the fixed array are refused before anything runs.
+check it against verify_attn with a fresh caller workspace, bit for bit (the
+same kernels run on the same inputs), on two calls in a row of different
+sizes -- a large one, then a smaller one that would expose anything the first
+left behind in the shared array; and check that sizes whose scratch would
+not fit the fixed array are refused before anything runs.
 
 This file is named so that pytest collects it last."""
 import numpy as np
@@ -21,39 +23,50 @@ from gpu_util import SM_SCALE, bf16_dev, fill_both, i32_dev
 pytestmark = pytest.mark.gpu
 
 
-def _close(got: np.ndarray, ref: np.ndarray) -> None:
-    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
-    assert (err <= 2e-3 + 1e-2 * np.abs(ref)).all(), float(err.max())
-
-
-@pytest.mark.parametrize("dtype,lens,W", [(synth.KV_FP8, [3000, 700, 12000], 16), (synth.KV_INT4, [5000, 64], 8)])
-def test_noalloc_matches_workspace_call_twice(dtype, lens, W):
-    import speculative_decode_verify_append_gb300 as sdva
-
-    spec = synth.Spec("noalloc", 31, len(lens), 0, 0, 24, 4, W, dtype, None, 0.7, True)
+def _case(dtype, lens, W, seed):
+    spec = synth.Spec("noalloc", seed, len(lens), 0, 0, 24, 4, W, dtype, None, 0.7, True)
     step = synth.make_step(spec, seq_lens=np.array(lens, np.int32), with_accept=False)
     gcache, _, _ = fill_both(spec, step, with_oracle=False)
-    B, Hq = len(lens), 24
-    max_context = max(lens)
-    q, table, seq = bf16_dev(step.q), i32_dev(step.page_table), i32_dev(step.seq_lens)
+    return spec, step, gcache
 
-    ws = torch.zeros(sdva.verify_attn_workspace_size(B, W, Hq, 4, max_context), dtype=torch.uint8, device="cuda")
+
+def _reference(sdva, gcache, step, q, table, seq, max_context):
+    """verify_attn with a freshly allocated workspace filled with NaN bytes."""
+    B, W, Hq = step.q.shape[:3]
+    n = sdva.verify_attn_workspace_size(B, W, Hq, 4, max_context)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
     ref = torch.empty((B, W, Hq, 128), dtype=torch.bfloat16, device="cuda")
-    st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
-    sdva.verify_attn(gcache, q, table, seq, max_context, float(SM_SCALE), ref, ws, st_ref)
-
-    outs = []
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for _ in range(2):  # the second call reuses the array as the first left it
-        out = torch.full((B, W, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
-        sdva.verify_attn_noalloc(gcache, q, table, seq, max_context, float(SM_SCALE), out, st)
-        outs.append(out)
+    sdva.verify_attn(gcache, q, table, seq, max_context, float(SM_SCALE), ref, ws, st)
     torch.cuda.synchronize()
-    assert int(st_ref.item()) == 0 and int(st.item()) == 0
-    r = ref.float().cpu().numpy()
-    assert np.isfinite(r).all()
-    for out in outs:
-        _close(out.float().cpu().numpy(), r)
+    assert int(st.item()) == 0
+    return ref
+
+
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+def test_noalloc_matches_workspace_call_large_then_small(dtype):
+    """Two calls in a row through the C ABI: first a large case (8 lanes up to
+    60,000 tokens, the scratch filled with its split-K partials), then a
+    smaller, different one (3 short lanes, other splits), so that a partial
+    left over from the first call would show in the second.  Each equals
+    verify_attn with a fresh NaN-filled workspace bit for bit: the two run
+    the same kernels on the same inputs."""
+    import speculative_decode_verify_append_gb300 as sdva
+
+    cases = [([3000, 700, 12000, 60000, 64, 9000, 31000, 150], 16, 31), ([500, 64, 1300], 8, 32)]
+    for lens, W, seed in cases:
+        spec, step, gcache = _case(dtype, lens, W if dtype == synth.KV_FP8 else min(W, 8), seed)
+        B, Wn, Hq = step.q.shape[:3]
+        max_context = max(lens)
+        q, table, seq = bf16_dev(step.q), i32_dev(step.page_table), i32_dev(step.seq_lens)
+        out = torch.full((B, Wn, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdva.verify_attn_noalloc(gcache, q, table, seq, max_context, float(SM_SCALE), out, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref = _reference(sdva, gcache, step, q, table, seq, max_context)
+        assert torch.isfinite(ref.float()).all()
+        assert torch.equal(out, ref), (lens, float((out.float() - ref.float()).abs().max()))
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
