@@ -59,7 +59,8 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": None, "bytes": {}}
+NCU_TRAFFIC = {"sources_sha256": "5119446dc563f5658948904fcdc2e192199192b2615caf0993d71fd444642c8e",
+               "bytes": {"multi_lane": 314576128, "long_context": 249101824}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
