@@ -80,8 +80,10 @@ def ncu_traffic(name: str):
 
 
 def workload_desc(spec: synth.Spec) -> str:
-    kv = "FP8 E4M3 KV, fp32 scale per (page, head)" if spec.kv_dtype == synth.KV_FP8 else \
-        "INT4 KV, fp16 scale per group of 32"
+    kv = {synth.KV_FP8: "FP8 E4M3 KV, fp32 scale per (page, head)",
+          synth.KV_INT4: "INT4 KV, fp16 scale per group of 32",
+          synth.KV_INT8: "INT8 KV, fp16 scale per group of 64",
+          synth.KV_FP8_ROW: "FP8 E4M3 KV, fp32 scale per (token, head) row"}[spec.kv_dtype]
     ctx = f"context {spec.ctx_lo}" if spec.ctx_lo == spec.ctx_hi else f"contexts U[{spec.ctx_lo}, {spec.ctx_hi}]"
     acc = f", acceptance over vocab {spec.vocab} (p={spec.match_p})" if spec.vocab else ""
     return (f"{spec.name}: {spec.num_lanes} lanes, {ctx}, {spec.num_q_heads} q / {spec.num_kv_heads} kv heads, "
@@ -96,11 +98,29 @@ def verify_algorithmic_bytes(spec: synth.Spec, seq_lens: np.ndarray) -> int:
     tokens = int(np.sum(seq_lens.astype(np.int64) + W))
     pages = int(np.sum((seq_lens.astype(np.int64) + W + 63) // 64))
     if spec.kv_dtype == synth.KV_FP8:
-        kv = tokens * Hkv * 256 + pages * Hkv * 8
+        kv = tokens * Hkv * 256 + pages * Hkv * 8          # E4M3 codes; fp32 K and V scale per page
+    elif spec.kv_dtype == synth.KV_INT4:
+        kv = tokens * Hkv * (128 + 16)                      # nibbles; 4 fp16 scales each for K and V
+    elif spec.kv_dtype == synth.KV_INT8:
+        kv = tokens * Hkv * (256 + 8)                       # int8 codes; 2 fp16 scales each for K and V
     else:
-        kv = tokens * Hkv * (128 + 16)
+        kv = tokens * Hkv * (256 + 8)                       # E4M3 codes; one fp32 scale each for K and V
     qo = 2 * len(seq_lens) * W * Hq * 128 * 2
     return kv + qo + pages * 4 + len(seq_lens) * 4
+
+
+KV_LABELS = {synth.KV_FP8: "fp8", synth.KV_INT4: "int4", synth.KV_INT8: "int8-g64", synth.KV_FP8_ROW: "fp8-row"}
+
+
+def all_workload_specs() -> dict:
+    """Every workload, plus the 8-lane workload in the INT8 group-64 and FP8
+    row-scale cache formats (same lengths, values and shapes)."""
+    import dataclasses
+    specs = dict(synth.WORKLOADS)
+    base = synth.WORKLOADS["multi_lane"]
+    for dt, tag in ((synth.KV_INT8, "int8"), (synth.KV_FP8_ROW, "fp8row")):
+        specs[f"multi_lane_{tag}"] = dataclasses.replace(base, name=f"multi_lane_{tag}", kv_dtype=dt)
+    return specs
 
 
 def measured_peaks() -> dict:
@@ -613,8 +633,8 @@ def run_gpu(args):
     all_workloads = None
     if not args.no_all_workloads:
         all_workloads = {}
-        for name in synth.WORKLOADS:
-            w = wl if name == spec.name else GpuWorkload(synth.WORKLOADS[name], dev)
+        for name, wspec in all_workload_specs().items():
+            w = wl if name == spec.name else GpuWorkload(wspec, dev)
             e_sep = time_loop(w.separate, args.steps, args.warmup, flush_l2, 4)
             e_ch = time_loop(lambda e: chained_step(e, w), args.steps, args.warmup, flush_l2)
             assert int(w.vs.status.item()) == 0, (name, sdva.sdva_status_string(int(w.vs.status.item())))
@@ -624,7 +644,7 @@ def run_gpu(args):
             gbs = w.alg / (v_us / 1e6) / 1e9
             all_workloads[name] = {"verify_attn_us": v_us, "verify_attn_gbs": gbs, "frac": gbs / peak,
                                    "algorithmic_bytes": w.alg, "step_us": st_us, "steps_per_s": 1e6 / st_us,
-                                   "separate_calls_step_us": sep_us, "kv": "int4" if w.spec.kv_dtype else "fp8"}
+                                   "separate_calls_step_us": sep_us, "kv": KV_LABELS[w.spec.kv_dtype]}
             if w is not wl:
                 del w
                 torch.cuda.empty_cache()
@@ -633,7 +653,8 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8-e4m3 KV (int4 for the 4-bit workload) -> f16 tensor-core MMA, f32 accumulate, bf16 out",
+        "dtype": "fp8-e4m3 KV (int4 for the 4-bit workload; int8 / fp8-row variants in all_workloads) -> "
+                 "f16 tensor-core MMA, f32 accumulate, bf16 out",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, N(0,1) fp32 logits)",
         "config": bench_config(spec, step.seq_lens, world),
         "step": "verify_step: kv_append_quant + verify_attn + spec_accept as one chain of programmatic dependent "

@@ -69,6 +69,22 @@
  *                        one scale per token and group of 32 head dims
  *     s = fp16_rne(min(amax_group / 7, 65504)); code = clamp(rint(x / s), -7, 7)
  *     with halves to even; value = code * s.
+ *   SDVA_KV_INT8_G64 (the same review section's "INT8 group-64"):
+ *     k_codes, v_codes : int8   [num_pages][num_kv_heads][64][128]  two's complement
+ *     k_scales, v_scales: fp16 bits [num_pages][num_kv_heads][64][2]
+ *                        one scale per token and group of 64 head dims
+ *     s = fp16_rne(min(amax_group / 127, 65504)); code = clamp(rint(x / s), -127, 127)
+ *     with halves to even; value = code * s.
+ *   SDVA_KV_FP8_ROW (the same section's "FP8 E4M3 row-256", read as one
+ *   scale per row of a token's head, 128 dims here):
+ *     k_codes, v_codes : uint8  [num_pages][num_kv_heads][64][128]  OCP E4M3
+ *     k_scales, v_scales: float [num_pages][num_kv_heads][64]  one per token
+ *     s = amax_row / 448 (fp32 IEEE division); code = e4m3_rne_sat(x / s); a
+ *     zero scale gives zero codes.  Every token carries its own scale, so
+ *     nothing is re-encoded.
+ *   The four arrays must be 16-byte aligned (else SDVA_ERR_INVALID).
+ *   verify_attn reads INT4, INT8 and FP8-row caches through fp16 (see
+ *   there): a dequantised value above 65504 in magnitude is out of range.
  *   page_table: int32 [num_lanes][max_pages_per_lane]; entry p of lane b is
  *     the physical page holding the lane's tokens [64p, 64p + 64).
  *   seq_lens: int32 [num_lanes], L_b = tokens already cached for lane b
@@ -88,7 +104,12 @@ extern "C" {
 /* Same type as cudaStream_t; NULL selects the legacy default stream. */
 typedef struct CUstream_st* sdva_stream_t;
 
-typedef enum { SDVA_KV_FP8_E4M3 = 0, SDVA_KV_INT4_G32 = 1 } sdva_kv_dtype;
+typedef enum {
+    SDVA_KV_FP8_E4M3 = 0, /* one fp32 scale per (page, kv head) */
+    SDVA_KV_INT4_G32 = 1, /* one fp16 scale per (token, kv head, 32 dims) */
+    SDVA_KV_INT8_G64 = 2, /* one fp16 scale per (token, kv head, 64 dims) */
+    SDVA_KV_FP8_ROW = 3   /* one fp32 scale per (token, kv head) */
+} sdva_kv_dtype;
 
 /* Description of a caller-owned cache; all four arrays are device memory
  * laid out as above. */
@@ -183,6 +204,12 @@ size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, in
  * max_pages_per_lane gets SDVA_STATUS_OVERFLOW; a lane with an invalid page id
  * among its first ceil((L_b + window) / 64) entries gets SDVA_STATUS_BAD_PAGE;
  * the output rows of such a lane are set to zero.
+ * Formats: FP8 keys enter the tensor core as stored codes; INT4 and INT8 K
+ * and V are widened to fp16 (code * scale, one rounding); FP8-row V is
+ * widened to fp16 as code * (s_j / s_max), s_max the largest V row scale of
+ * the page's written rows, so a row whose scale is below 2^-14 s_max keeps
+ * fewer significant bits (fp16 subnormals).  INT8 and FP8-row need at most
+ * 128 rows per kv head (window * Hq / Hkv <= 128; else SDVA_ERR_UNSUPPORTED).
  * Returns SDVA_OK or a negative SDVA_ERR_*.
  */
 int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,

@@ -39,6 +39,8 @@ LIB_PATH = os.path.join(_PKG, "libsdva.so")
 
 KV_FP8_E4M3 = 0
 KV_INT4_G32 = 1
+KV_INT8_G64 = 2
+KV_FP8_ROW = 3
 PAGE = 64
 HEAD_DIM = 128
 MAX_WINDOW = 16
@@ -170,6 +172,8 @@ class KVCache:
 
     FP8:  k_codes/v_codes uint8 [pages][Hkv][64][128]; k_scales/v_scales float32 [pages][Hkv]
     INT4: k_codes/v_codes uint8 [pages][Hkv][64][64];  k_scales/v_scales float16 [pages][Hkv][64][4]
+    INT8: k_codes/v_codes uint8 (int8 bits) [pages][Hkv][64][128]; k_scales/v_scales float16 [pages][Hkv][64][2]
+    FP8_ROW: k_codes/v_codes uint8 [pages][Hkv][64][128]; k_scales/v_scales float32 [pages][Hkv][64]
     """
 
     def __init__(self, dtype: int, num_pages: int, num_kv_heads: int, device="cuda", tensors=None):
@@ -184,13 +188,20 @@ class KVCache:
             self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
             self.k_scales = torch.zeros((num_pages, num_kv_heads), dtype=torch.float32, device=device)
             self.v_scales = torch.zeros((num_pages, num_kv_heads), dtype=torch.float32, device=device)
-        elif self.dtype == KV_INT4_G32:
-            shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 2)
-            sshape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 32)
+        elif self.dtype in (KV_INT4_G32, KV_INT8_G64, KV_FP8_ROW):
+            if self.dtype == KV_INT4_G32:
+                shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 2)
+                sshape, sdt = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 32), torch.float16
+            elif self.dtype == KV_INT8_G64:
+                shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
+                sshape, sdt = (num_pages, num_kv_heads, PAGE, HEAD_DIM // 64), torch.float16
+            else:
+                shape = (num_pages, num_kv_heads, PAGE, HEAD_DIM)
+                sshape, sdt = (num_pages, num_kv_heads, PAGE), torch.float32
             self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
             self.v_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
-            self.k_scales = torch.zeros(sshape, dtype=torch.float16, device=device)
-            self.v_scales = torch.zeros(sshape, dtype=torch.float16, device=device)
+            self.k_scales = torch.zeros(sshape, dtype=sdt, device=device)
+            self.v_scales = torch.zeros(sshape, dtype=sdt, device=device)
         else:
             raise ValueError(f"unknown kv dtype {dtype}")
 

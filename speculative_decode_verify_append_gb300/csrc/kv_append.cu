@@ -4,11 +4,14 @@
 // FP8 E4M3 cache with one fp32 scale per (page, kv head): the KV format the
 // NInfer review names in section "성능과 평가" ("FP8 E4M3" KV).  INT4 cache with
 // an fp16 scale per token and group of 32 head dims: the 4-bit KV setting of
-// the MegaCapybara announcement, item 2.  The scale rules (a page's FP8 scale
-// only grows while it fills; growth re-encodes the page's earlier tokens) are
-// the reading this library takes; they are spelled out in sdva.h.
+// the MegaCapybara announcement, item 2.  INT8 with an fp16 scale per token
+// and group of 64 dims, and FP8 E4M3 with an fp32 scale per token row: the
+// "INT8 group-64" and "FP8 E4M3 row-256" records of the same review section.
+// The scale rules (a page's FP8 scale only grows while it fills; growth
+// re-encodes the page's earlier tokens; the per-token formats never
+// re-encode) are the reading this library takes; they are spelled out in sdva.h.
 //
-// Both kernels are launch-bound (a verify window is at most 16 tokens, 64 KB
+// The kernels are launch-bound (a verify window is at most 16 tokens, 64 KB
 // of bf16 input at 12 lanes): one CTA per (touched page, lane[, kv head, K|V]),
 // 16-byte vector loads and stores, fp32 arithmetic through explicitly rounded
 // intrinsics (__fdiv_rn / __fmul_rn) so that no contraction or approximate
@@ -217,6 +220,84 @@ __global__ void __launch_bounds__(kAppendThreads) append_int4_kernel(AppendArgs 
   }
 }
 
+// grid: (touched-page slot, lane).  INT8 group-64 and FP8 row formats: every
+// token carries its own scales, so each row is quantised on its own.  Eight
+// threads per (token, kv head, K|V) row, 16 dims each (two 16-byte loads, one
+// 16-byte store of codes); the amax of the row (FP8 row) or of each 64-dim
+// group (INT8) is reduced over the row's threads with shuffles.
+template <bool kFp8Row>
+__global__ void __launch_bounds__(kAppendThreads) append_rowscaled_kernel(AppendArgs a) {
+  // a kernel launched as this one's programmatic dependent may be scheduled
+  // now; it waits (griddepcontrol.wait) before it reads the cache
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int slot = blockIdx.x, b = blockIdx.y;
+  const int n = lane_tokens(a, b, slot == 0);
+  if (n == 0) return;  // nothing to write: the lane is not examined
+  const int L = a.seq_lens[b];
+  if (!lane_admitted(a, b, L, n, slot == 0)) return;
+  const int lp = L / kPage + slot;
+  if ((long long)lp * kPage >= (long long)L + n) return;
+  const int pid = a.page_table[(size_t)b * a.max_pages + lp];
+  const int t0 = max(L, lp * kPage), t1 = min(L + n, lp * kPage + kPage);
+  const int count = t1 - t0;
+  const int H = a.num_kv_heads;
+  const size_t token_stride = (size_t)H * kHeadDim;
+  // The item count is a multiple of 8 and a row's 8 items are 8 aligned
+  // lanes of one warp, so a row's threads enter and leave the loop together.
+  const unsigned row_mask = 0xFFu << (threadIdx.x & 24);
+  for (int it = threadIdx.x; it < count * H * 16; it += blockDim.x) {
+    const int sub = it & 7, is_v = (it >> 3) & 1, rest = it >> 4;
+    const int hk = rest % H, t = rest / H;
+    const int off = t0 + t - lp * kPage;
+    const uint16_t* src = (is_v ? a.v_new : a.k_new) + ((size_t)b * a.n_new + (t0 - L + t)) * token_stride +
+                          (size_t)hk * kHeadDim + sub * 16;
+    float x[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(src)[q];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[q * 8 + 2 * j] = bf16_lo(w[j]);
+        x[q * 8 + 2 * j + 1] = bf16_hi(w[j]);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    // over the 4 threads of a 64-dim group, then (FP8 row) over both groups
+    amax = fmaxf(amax, __shfl_xor_sync(row_mask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(row_mask, amax, 2));
+    if (kFp8Row) amax = fmaxf(amax, __shfl_xor_sync(row_mask, amax, 4));
+    const size_t row = ((size_t)pid * H + hk) * kPage + off;  // (page, kv head, token) row
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if constexpr (kFp8Row) {
+      const float s = __fdiv_rn(amax, 448.0f);
+      if (s != 0.0f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          packed[j] = e4m3x2_from_f32(__fdiv_rn(x[4 * j], s), __fdiv_rn(x[4 * j + 1], s)) |
+                      ((uint32_t)e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s), __fdiv_rn(x[4 * j + 3], s)) << 16);
+      }
+      if (sub == 0) reinterpret_cast<float*>(is_v ? a.v_scales : a.k_scales)[row] = s;
+    } else {
+      const __half s16 = __float2half_rn(fminf(__fdiv_rn(amax, 127.0f), 65504.0f));
+      const float sf = __half2float(s16);
+      if (sf != 0.0f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          int qv = __float2int_rn(__fdiv_rn(x[j], sf));
+          qv = max(-127, min(127, qv));
+          packed[j >> 2] |= (uint32_t)(qv & 0xFF) << (8 * (j & 3));
+        }
+      }
+      if ((sub & 3) == 0) reinterpret_cast<__half*>(is_v ? a.v_scales : a.k_scales)[row * 2 + (sub >> 2)] = s16;
+    }
+    *reinterpret_cast<uint4*>((is_v ? a.v_codes : a.k_codes) + row * kHeadDim + sub * 16) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
 }  // namespace
 }  // namespace sdva
 
@@ -234,7 +315,8 @@ int sdva::append_launch(const sdva_kv_cache* cache, const void* k_new, const voi
       cache->num_kv_heads <= 0)
     return SDVA_ERR_INVALID;
   if (cache->page_size != kPage || cache->head_dim != kHeadDim) return SDVA_ERR_UNSUPPORTED;
-  if (cache->dtype != SDVA_KV_FP8_E4M3 && cache->dtype != SDVA_KV_INT4_G32) return SDVA_ERR_UNSUPPORTED;
+  if (cache->dtype < SDVA_KV_FP8_E4M3 || cache->dtype > SDVA_KV_FP8_ROW) return SDVA_ERR_UNSUPPORTED;
+  if (!cache_aligned(cache)) return SDVA_ERR_INVALID;
   if (num_lanes > 65535 || cache->num_kv_heads > 32767) return SDVA_ERR_UNSUPPORTED;
   if (check_only) return SDVA_OK;
   AppendArgs a;
@@ -256,8 +338,12 @@ int sdva::append_launch(const sdva_kv_cache* cache, const void* k_new, const voi
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cache->dtype == SDVA_KV_FP8_E4M3) {
     append_fp8_kernel<<<dim3(slots, num_lanes, cache->num_kv_heads * 2), kAppendThreads, 0, s>>>(a);
-  } else {
+  } else if (cache->dtype == SDVA_KV_INT4_G32) {
     append_int4_kernel<<<dim3(slots, num_lanes), kAppendThreads, 0, s>>>(a);
+  } else if (cache->dtype == SDVA_KV_INT8_G64) {
+    append_rowscaled_kernel<false><<<dim3(slots, num_lanes), kAppendThreads, 0, s>>>(a);
+  } else {
+    append_rowscaled_kernel<true><<<dim3(slots, num_lanes), kAppendThreads, 0, s>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? SDVA_OK : SDVA_ERR_CUDA;
 }

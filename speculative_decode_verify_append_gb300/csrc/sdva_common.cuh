@@ -20,6 +20,13 @@ __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
 
+// The cache arrays are read and written with 16-byte vectors and bulk copies.
+inline bool cache_aligned(const sdva_kv_cache* c) {
+  return ((reinterpret_cast<uintptr_t>(c->k_codes) | reinterpret_cast<uintptr_t>(c->v_codes) |
+           reinterpret_cast<uintptr_t>(c->k_scales) | reinterpret_cast<uintptr_t>(c->v_scales)) &
+          15u) == 0;
+}
+
 // ---------------------------------------------------------------------------
 // FP8 E4M3 (OCP, "fn")
 // ---------------------------------------------------------------------------

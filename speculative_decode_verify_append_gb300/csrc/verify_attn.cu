@@ -487,7 +487,8 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
     return SDVA_ERR_INVALID;
   if (!(sm_scale > 0.0f) || !isfinite(sm_scale)) return SDVA_ERR_INVALID;
   if (cache->page_size != kPage || cache->head_dim != kHeadDim || window > kMaxWindow) return SDVA_ERR_UNSUPPORTED;
-  if (cache->dtype != SDVA_KV_FP8_E4M3 && cache->dtype != SDVA_KV_INT4_G32) return SDVA_ERR_UNSUPPORTED;
+  if (cache->dtype < SDVA_KV_FP8_E4M3 || cache->dtype > SDVA_KV_FP8_ROW) return SDVA_ERR_UNSUPPORTED;
+  if (!cache_aligned(cache)) return SDVA_ERR_INVALID;
   const int num_sms = device_sm_count();
   VerifyPlan plan;
   if (num_sms <= 0) return SDVA_ERR_CUDA;
@@ -498,7 +499,7 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (tc::tc_supported(cache, num_lanes, window, num_q_heads, max_pages_per_lane, num_sms)) {
-    // <= 128 rows per kv head: tcgen05 kernels (FP8 or INT4 cache)
+    // <= 128 rows per kv head: tcgen05 kernels (every cache format)
     if (workspace_bytes < tc::tc_workspace_bytes(num_lanes, window, num_q_heads, cache->num_kv_heads, num_sms))
       return SDVA_ERR_WORKSPACE;
     if (check_only) return SDVA_OK;
@@ -531,8 +532,10 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
     t.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     return tc::launch_verify_tc(cache, t, num_sms, s, after_append);
   }
-  // the mma.sync kernels (more than 128 rows per kv head) know only the causal window
+  // the mma.sync kernels (more than 128 rows per kv head) know only the
+  // causal window and the FP8 page-scale and INT4 formats
   if (parent != nullptr || n_lane != nullptr) return SDVA_ERR_UNSUPPORTED;
+  if (cache->dtype != SDVA_KV_FP8_E4M3 && cache->dtype != SDVA_KV_INT4_G32) return SDVA_ERR_UNSUPPORTED;
   if (workspace_bytes < plan.bytes) return SDVA_ERR_WORKSPACE;
   if (check_only) return SDVA_OK;
 

@@ -51,10 +51,9 @@ namespace sdva {
 namespace tc {
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 8;            // code stages, at most (INT8 holds fewer)
 constexpr int kTileBytes = 8192;     // FP8: 64 rows x 128 E4M3 codes
-constexpr int kI4Codes = 4096;       // INT4: 64 rows x 64 code bytes
-constexpr int kI4Scales = 512;       // INT4: 64 rows x 4 fp16 group scales
+constexpr int kRowScaleBytes = 512;  // FP8 row: 64 fp32 K scales | 64 fp32 V scales
 constexpr int kV16Stages = 3;
 constexpr int kQBytes = 32768;       // Q operand: FP8 Q_hi | Q_lo (128 rows x 128 B each), or fp16 (dims 0-63 | 64-127)
 constexpr int kV16Bytes = 16384;     // fp16 K or V of one page: dims 0-63 | dims 64-127, 64 rows x 128 B each
@@ -63,18 +62,28 @@ constexpr int kQkWarp = 9;           // + warpgroup index
 constexpr int kPvWarp = 11;
 constexpr int kConvWarp = 12;        // converters: warps 12-15
 constexpr int kThreads = 16 * 32;
-// Shared memory: the fp16 V ring, the fp16 K ring (INT4 only), the K/V code
-// stages, then Ctl.  A stage holds one (page, kv head): FP8 K and V tiles
-// (TMA, 128-byte swizzle), or INT4 K codes, V codes, K scales, V scales.
+// Shared memory: the fp16 V ring, the fp16 K ring (INT4 and INT8), the K/V
+// code stages, the row-scale stages (FP8 row), then Ctl.  A stage holds one
+// (page, kv head): FP8 K and V tiles (TMA, 128-byte swizzle, 1024-byte
+// aligned), or INT4 / INT8 K codes, V codes, K scales, V scales as stored.
 template <int KVT>
 struct Smem {
   static constexpr bool kInt4 = KVT == SDVA_KV_INT4_G32;
-  static constexpr uint32_t kStageBytes = kInt4 ? 2 * kI4Codes + 2 * kI4Scales : 2 * kTileBytes;
+  static constexpr bool kInt8 = KVT == SDVA_KV_INT8_G64;
+  static constexpr bool kRow = KVT == SDVA_KV_FP8_ROW;
+  // K and V widened to fp16 (code * scale) by the converters; the QK MMA is
+  // then kind::f16 against fp16 Q
+  static constexpr bool kDeq = kInt4 || kInt8;
+  static constexpr uint32_t kCodeBytes = kInt4 ? 4096 : 8192;  // per K or V page: 64 rows of codes
+  static constexpr uint32_t kScaleBytes = kInt4 ? 512 : 256;   // INT4 / INT8: 64 rows of fp16 group scales
+  static constexpr uint32_t kStageBytes = kDeq ? 2 * kCodeBytes + 2 * kScaleBytes : 2 * kTileBytes;
+  static constexpr int kNumStages = kInt8 ? 5 : kStages;
   static constexpr uint32_t kOffV16 = 0;
   static constexpr uint32_t kOffK16 = kOffV16 + kV16Stages * kV16Bytes;
-  static constexpr uint32_t kOffQ = kOffK16 + (kInt4 ? kV16Stages * kV16Bytes : 0);
+  static constexpr uint32_t kOffQ = kOffK16 + (kDeq ? kV16Stages * kV16Bytes : 0);
   static constexpr uint32_t kOffStages = kOffQ + kQBytes;
-  static constexpr uint32_t kOffCtl = kOffStages + kStages * kStageBytes;
+  static constexpr uint32_t kOffRowSc = kOffStages + kNumStages * kStageBytes;
+  static constexpr uint32_t kOffCtl = kOffRowSc + (kRow ? kNumStages * kRowScaleBytes : 0);
 };
 // Register split: launched at 128 per thread (65536 for the block); the two
 // softmax warpgroups grow to kRegsSoftmax, the other two shrink to kRegsOther.
@@ -114,6 +123,7 @@ struct Ctl {
   int bad1;                 // warpgroup 1 met such a page in the current segment
   float shift[kStages];     // log2 of its V scale (0 when the scale is 0)
   float inv_v[kStages];     // 1 / V scale (1 when the scale is 0)
+  int nv[kStages];          // FP8 row: rows of the page written (the lane's tokens in it)
   float m1[128];            // warpgroup 1's running max / sum at the end of a segment
   float l1[128];
   uint32_t tmem_base;
@@ -131,6 +141,10 @@ constexpr size_t smem_bytes() {
 }
 static_assert(smem_bytes<SDVA_KV_FP8_E4M3>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<SDVA_KV_INT4_G32>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<SDVA_KV_INT8_G64>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<SDVA_KV_FP8_ROW>() <= 232448, "shared memory budget");
+static_assert(Smem<SDVA_KV_FP8_ROW>::kOffStages % 1024 == 0 && Smem<SDVA_KV_FP8_E4M3>::kOffStages % 1024 == 0,
+              "TMA tiles with the 128-byte swizzle start on 1024-byte boundaries");
 
 // Partition of the flattened (lane, kv head, page) list over the CTAs.  Each
 // unit (lane, kv head) costs its pages plus kUnitCost: a CTA that starts a
@@ -400,6 +414,38 @@ __device__ __forceinline__ void int4_group_to_f16(uint4 codes, uint32_t scale_bi
   }
 }
 
+// Sixteen INT8 codes (dims 16c .. 16c + 15 of a row, one 64-dim group) times
+// the group's fp16 scale -> fp16, dims in order two per word.  The int8 ->
+// fp16 step is exact: with its sign bit flipped a code q is the byte q + 128,
+// placed under the fp16 exponent of 1024 (0x6400 | byte) it reads 1152 + q,
+// and subtracting 1152 leaves q.  The product is the one rounding.
+__device__ __forceinline__ void int8x16_to_f16(uint4 codes, uint32_t scale_bits, uint32_t (&out)[8]) {
+  const __half2 s2 = __halves2half2(__ushort_as_half((unsigned short)scale_bits),
+                                    __ushort_as_half((unsigned short)scale_bits));
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t ob = cw[k] ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(ob, 0x64646464u, 0x4140);  // dims 4k, 4k + 1
+    const uint32_t hi = __byte_perm(ob, 0x64646464u, 0x4342);  // dims 4k + 2, 4k + 3
+    const __half2 v0 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), s2);
+    const __half2 v1 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), s2);
+    out[2 * k] = *reinterpret_cast<const uint32_t*>(&v0);
+    out[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&v1);
+  }
+}
+
+// FP8 row format: the largest V row scale among the first nv rows of a
+// stage's page (zero when there is none), computed by a whole warp from the
+// row-scale stage (V scales at entries 64 .. 127).
+__device__ __forceinline__ float row_vscale_max(const float* rs, int nv, int lane) {
+  float m = fmaxf(lane < nv ? rs[64 + lane] : 0.0f, lane + 32 < nv ? rs[96 + lane] : 0.0f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
 // kMode: bit 0 -- draft-tree window (a.parent); bit 1 -- a window row count
 // per lane (a.n_lane).  Mode 0, the causal window, is the common case.
 constexpr int kModeTree = 1, kModeRagged = 2;
@@ -412,9 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   using SM = Smem<KVT>;
-  constexpr bool kInt4 = SM::kInt4;
+  constexpr bool kDeq = SM::kDeq, kRow = SM::kRow;
+  constexpr int kNS = SM::kNumStages;
   constexpr bool kTree = (kMode & kModeTree) != 0, kRagged = (kMode & kModeRagged) != 0;
-  constexpr bool kSpinWait = !kInt4;  // see mbar_wait
+  constexpr bool kSpinWait = !kDeq;  // see mbar_wait (the converters need the issue slots)
   constexpr uint32_t kStageBytes = SM::kStageBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(base_ptr + SM::kOffCtl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -435,13 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   // only the softmax warps that own query rows take part in the page protocol
   const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kNS; ++s) {
       // FP8: the copies' expect_tx arrival, then the scale terms; INT4: the
       // copies' arrival (the scales are inside the stage)
-      mbar_init(smem_u32(&ctl->full[s]), kInt4 ? 1 : 2);
+      mbar_init(smem_u32(&ctl->full[s]), kDeq ? 1 : 2);
       // FP8: QK commit (K tile), converters (V tile), softmax warps (scales);
       // INT4: converters (K and V codes), softmax warps
-      mbar_init(smem_u32(&ctl->empty[s]), (kInt4 ? 0 : 1) + 4 + row_threads / 32);
+      mbar_init(smem_u32(&ctl->empty[s]), (kDeq ? 0 : 1) + 4 + row_threads / 32);
     }
     for (int t = 0; t < kV16Stages; ++t) {
       mbar_init(smem_u32(&ctl->v16_full[t]), 4);
@@ -485,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     // producer: page ids and scales prefetched 32 pages at a time, two
     // batches ahead; lane 0 issues the TMA loads.
     // ------------------------------------------------------------------
-    if constexpr (!kInt4) {
+    if constexpr (!kDeq) {
       prefetch_tmap(&map_k);
       prefetch_tmap(&map_v);
     }
@@ -505,17 +552,29 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (pid < 0 || pid >= a.num_pages) return it.hk | kBadPage;
       return pid * a.Hkv + it.hk;
     };
-    // the page's scale terms for the softmax (INT4 scales are applied by the converters)
+    // the page's scale terms for the softmax (INT4 and INT8 scales are applied
+    // by the converters; FP8 row scales travel in the row-scale stage)
     auto k_scale_of = [&](int ph) -> float {
-      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.k_scales)[ph & ~kBadPage] : 0.0f);
+      return (kDeq || kRow) ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.k_scales)[ph & ~kBadPage] : 0.0f);
     };
     auto v_scale_of = [&](int ph) -> float {
-      return kInt4 ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph & ~kBadPage] : 0.0f);
+      return (kDeq || kRow) ? 1.0f : (ph >= 0 ? static_cast<const float*>(a.v_scales)[ph & ~kBadPage] : 0.0f);
+    };
+    // FP8 row: rows of the page at position g that hold the lane's tokens (up
+    // to L_b + the lane's window rows); the other rows' scales are not read
+    auto written_of = [&](long long g) -> int {
+      if (g >= n_local) return 0;
+      PageIter it;
+      it.seek(start + g, ctl->pref, a.B, a.Hkv);
+      int rows = a.W;
+      if constexpr (kRagged) rows = min(max(a.n_lane[it.b], 0), a.W);
+      const long long end = (long long)ctl->lens[it.b] + rows - (long long)it.p * kPage;
+      return (int)max(0LL, min((long long)kPage, end));
     };
     long long issued = 0;
     bool ok = true;
-    if constexpr (kInt4) {
-      // INT4: the scales travel inside the stage (applied by the converters)
+    if constexpr (kDeq) {
+      // INT4 / INT8: the scales travel inside the stage (applied by the converters)
       int ph_a = locate(lane), ph_b = locate(32 + lane);
       for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
         const int ph_c = locate(g0 + 64 + lane);
@@ -523,9 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           const long long g = g0 + i;
           const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
           const int ph = ph_m & ~kBadPage;
-          const int s = (int)(g % kStages);
-          if (g >= kStages &&
-              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag, a.wait_limit)))
+          const int s = (int)(g % kNS);
+          if (g >= kNS &&
+              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kNS - 1) & 1), abort_flag, a.wait_limit)))
             break;
           if (lane == 0) {
             const int page_bad = (ph_m & kBadPage) ? 1 : 0;
@@ -538,12 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
             const uint32_t dst = stages + s * kStageBytes;
             mbar_arrive_expect_tx(bar, kStageBytes);
             // K codes | V codes | K scales | V scales, each contiguous per (page, kv head)
-            bulk_load(dst, a.k_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
-            bulk_load(dst + kI4Codes, a.v_codes + (size_t)ph * kI4Codes, kI4Codes, bar);
-            bulk_load(dst + 2 * kI4Codes, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * kI4Scales,
-                      kI4Scales, bar);
-            bulk_load(dst + 2 * kI4Codes + kI4Scales,
-                      static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * kI4Scales, kI4Scales, bar);
+            constexpr uint32_t kC = SM::kCodeBytes, kS = SM::kScaleBytes;
+            bulk_load(dst, a.k_codes + (size_t)ph * kC, kC, bar);
+            bulk_load(dst + kC, a.v_codes + (size_t)ph * kC, kC, bar);
+            bulk_load(dst + 2 * kC, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * kS, kS, bar);
+            bulk_load(dst + 2 * kC + kS, static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * kS, kS, bar);
           }
           __syncwarp();
           issued = g + 1;
@@ -558,28 +616,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       for (long long g0 = 0; g0 < n_local && ok; g0 += 32) {
         const int ph_c = locate(g0 + 64 + lane);
         const float sk_b = k_scale_of(ph_b), sv_b = v_scale_of(ph_b);
+        const int nv_a = kRow ? written_of(g0 + lane) : 0;
         for (int i = 0; i < 32 && g0 + i < n_local; ++i) {
           const long long g = g0 + i;
           const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
           const int ph = ph_m & ~kBadPage;
-          const int s = (int)(g % kStages);
-          if (g >= kStages && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kStages - 1) & 1), abort_flag, a.wait_limit)))
+          const int s = (int)(g % kNS);
+          if (g >= kNS && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kNS - 1) & 1), abort_flag, a.wait_limit)))
             break;
           const uint32_t bar = smem_u32(&ctl->full[s]);
           if (lane == 0) {
             // the copies go out as soon as the page id is known; the stage's
             // scale terms follow with the barrier's second arrival
             const uint32_t dst = stages + s * kStageBytes;
-            mbar_arrive_expect_tx(bar, kStageBytes);
+            mbar_arrive_expect_tx(bar, kStageBytes + (kRow ? kRowScaleBytes : 0));
             tma_load_2d(dst, &map_k, 0, ph * kPage, bar);
             tma_load_2d(dst + kTileBytes, &map_v, 0, ph * kPage, bar);
+            if constexpr (kRow) {
+              // the page's 64 K and 64 V row scales (256 bytes each per (page, kv head))
+              const uint32_t rs = base + SM::kOffRowSc + s * kRowScaleBytes;
+              bulk_load(rs, static_cast<const uint8_t*>(a.k_scales) + (size_t)ph * 256, 256, bar);
+              bulk_load(rs + 256, static_cast<const uint8_t*>(a.v_scales) + (size_t)ph * 256, 256, bar);
+            }
           }
           const float sk = __shfl_sync(0xffffffffu, sk_a, i);
           const float sv = __shfl_sync(0xffffffffu, sv_a, i);
+          const int nv = __shfl_sync(0xffffffffu, nv_a, i);
           if (lane == 0) {
             const int page_bad = (ph_m & kBadPage) ? 1 : 0;
             if (page_bad) raise_status(a.status, SDVA_STATUS_BAD_PAGE);
             ctl->bad[s] = page_bad;
+            ctl->nv[s] = nv;
             ctl->sk[s] = sk;
             ctl->shift[s] = sv > 0.0f ? log2f(sv) : 0.0f;
             ctl->inv_v[s] = sv > 0.0f ? 1.0f / sv : 1.0f;
@@ -597,9 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     if (!ok) {
       fail(ctl, a.status);
       // drain this CTA's own copies still in flight (bounded)
-      for (long long g = max(0LL, issued - kStages); g < issued; ++g) {
+      for (long long g = max(0LL, issued - kNS); g < issued; ++g) {
         int dummy = 0;
-        mbar_wait<kSpinWait>(smem_u32(&ctl->full[g % kStages]), (uint32_t)((g / kStages) & 1), &dummy, 400000000LL);
+        mbar_wait<kSpinWait>(smem_u32(&ctl->full[g % kNS]), (uint32_t)((g / kNS) & 1), &dummy, 400000000LL);
       }
     }
   } else if (warp == kQkWarp || warp == kQkWarp + 1) {
@@ -620,10 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_full), q_phase, abort_flag, a.wait_limit))) break;
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
-        const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
+        const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
         // FP8: the page's K tile as loaded; INT4: its fp16 K from the converters
-        if (!(ok = kInt4 ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit)
-                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag, a.wait_limit)))
+        if (!(ok = kDeq ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit)
+                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kNS) & 1), abort_flag, a.wait_limit)))
           break;
         const long long n = h >> 1;  // the warpgroup's own page index
         const int x = (int)(n & 1);
@@ -633,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         fence_after_sync();
         if (lane == 0) {
           const uint32_t d = tmem + col_s(j, x);
-          if constexpr (kInt4) {
+          if constexpr (kDeq) {
             // kind::f16: Q and K as fp16 rows of 128 bytes per 64-dim half
             // (Q halves 16384 bytes apart, K halves 8192)
             const uint32_t kt = k16 + t * kV16Bytes;
@@ -735,17 +802,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     const int u = threadIdx.x - kConvWarp * 32;
     bool ok = true;
     for (long long h = 0; h < n_local && ok; ++h) {
-      const int s = (int)(h % kStages), t = (int)(h % kV16Stages);
-      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kStages) & 1), abort_flag, a.wait_limit))) break;
+      const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kNS) & 1), abort_flag, a.wait_limit))) break;
       if (h >= kV16Stages &&
           !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
-      if (kInt4 && h >= kV16Stages &&
+      if (kDeq && h >= kV16Stages &&
           !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
       const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
       uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
-      if constexpr (kInt4) {
+      if constexpr (SM::kInt8) {
+        // INT8: K and V, 64 rows x 8 chunks of 16 dims each; chunk (tk, r, c)
+        // -> 2 chunks of 8 dims in the swizzled fp16 layout (K: the K-major
+        // operand of the QK MMA; V: the MN-major operand of the PV MMA)
+        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
+#pragma unroll 4
+        for (int q = 0; q < 8; ++q) {
+          const int item = u + 128 * q;  // 1024 chunks per page
+          const int tk = item >> 9, r = (item >> 3) & 63, c = item & 7;
+          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 128 + c * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes +
+                                                                 r * 4 + (c >> 2) * 2);
+          uint32_t h16[8];
+          int8x16_to_f16(codes, sc, h16);
+          // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
+          uint8_t* reg = (tk ? dst : kdst) + (c >> 2) * 8192 + r * 128;
+          const int c0 = 2 * (c & 3);
+          *reinterpret_cast<uint4*>(reg + ((c0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+          *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+        }
+      } else if constexpr (kDeq) {
         // INT4: K and V, 64 rows x 4 groups of 32 dims each; group (tk, r, gi)
         // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
         // it is the K-major operand of the QK MMA)
@@ -754,8 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         for (int q = 0; q < 4; ++q) {
           const int item = u + 128 * q;  // 512 groups per page
           const int tk = item >> 8, r = (item >> 2) & 63, gi = item & 3;
-          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * kI4Codes + r * 64 + gi * 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * kI4Codes + tk * kI4Scales + r * 8 + gi * 2);
+          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
           uint4 ch[4];
           int4_group_to_f16(codes, sc, ch);
           // dims 32gi .. 32gi + 31 -> region gi >> 1, 8-dim chunks 4 (gi & 1) .. + 3
@@ -766,6 +853,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         }
       } else {
         const uint8_t* src = stage + kTileBytes;
+        // FP8 row: row r is widened as code * (s_r / s_max) (zero past the
+        // page's written rows); the softmax folds s_max into its shift
+        const float* rs = reinterpret_cast<const float*>(base_ptr + SM::kOffRowSc + s * kRowScaleBytes);
+        int nv = 0;
+        float inv_max = 0.0f;
+        if constexpr (kRow) {
+          nv = ctl->nv[s];
+          const float vmax = row_vscale_max(rs, nv, lane);
+          inv_max = vmax > 0.0f ? 1.0f / vmax : 0.0f;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
         const int item = u + 128 * q;
@@ -777,6 +874,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         for (int k = 0; k < 4; ++k) {
           h16[2 * k] = f16x2_from_e4m3x2(b[k] & 0xFFFFu);
           h16[2 * k + 1] = f16x2_from_e4m3x2(b[k] >> 16);
+        }
+        if constexpr (kRow) {
+          const __half2 f2 = __float2half2_rn(r < nv ? rs[64 + r] * inv_max : 0.0f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h16[k]), f2);
+            h16[k] = *reinterpret_cast<const uint32_t*>(&v);
+          }
         }
         // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
         uint8_t* reg = dst + (c >> 2) * 8192 + r * 128;
@@ -790,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&ctl->v16_full[t]));
-        if (kInt4) mbar_arrive(smem_u32(&ctl->k16_full[t]));
+        if (kDeq) mbar_arrive(smem_u32(&ctl->k16_full[t]));
         mbar_arrive(smem_u32(&ctl->empty[s]));
       }
     }
@@ -824,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       const int u = b * a.Hkv + hk;
       const int h = hk * a.G + (row_valid ? row % a.G : 0);
       const uint16_t* qrow = a.q + (((size_t)b * a.W + i_row) * a.Hq + h) * kHeadDim;
-      const int e = kInt4 ? (row_valid ? q_row_exponent(qrow) : 0) : q_row_exponent_ldg(row_valid ? qrow : nullptr);
+      const int e = kDeq ? (row_valid ? q_row_exponent(qrow) : 0) : q_row_exponent_ldg(row_valid ? qrow : nullptr);
       if (ok && wg == 0 && warp_active) {
         // the previous segment's QKs are all issued (and, through the
         // segment-end handshake, complete): Q may be overwritten
@@ -832,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (ok) {
           // Q into the shared-memory A operand of the QK MMAs
           uint8_t* qb = base_ptr + SM::kOffQ;
-          if constexpr (kInt4)
+          if constexpr (kDeq)
             store_q16_row_smem(row_valid ? qrow : nullptr, e, qb, row);
           else
             store_q_row_smem(row_valid ? qrow : nullptr, e, qb, qb + 16384, row);
@@ -886,22 +991,45 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if (!warp_active) continue;
         const int j = wg;
         const int p = p0 + (int)k;
-        const int s = (int)(g % kStages);
+        const int s = (int)(g % kNS);
         const long long n = g >> 1;  // this warpgroup's own page index
         const int xb = (int)(n & 1);  // its S buffer
         if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag, a.wait_limit))) break;
         // the producer staged the page's scale terms before completing full[s]
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kStages) & 1), abort_flag, a.wait_limit))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kNS) & 1), abort_flag, a.wait_limit))) break;
         fence_after_sync();
-        const float kscale = ctl->sk[s] * row_scale, shift = ctl->shift[s], inv_f = ctl->inv_v[s];
+        const float kscale = ctl->sk[s] * row_scale;
+        float shift = ctl->shift[s], inv_f = ctl->inv_v[s];
         seg_bad |= ctl->bad[s];
-        // the stage's scale terms are in registers: this warp's share of releasing the stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
+        if constexpr (!kRow) {
+          // the stage's scale terms are in registers: this warp's share of releasing the stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
+        }
         uint32_t x[64];
         tmem_ld32(lane_base + col_s(j, xb), *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
         tmem_ld32(lane_base + col_s(j, xb) + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
+        if constexpr (kRow) {
+          // FP8 row: score j times key j's K scale; the page's largest V row
+          // scale is the V scale folded into the shift (the converters
+          // divided it out of the fp16 V)
+          const float* rs = reinterpret_cast<const float*>(base_ptr + SM::kOffRowSc + s * kRowScaleBytes);
+          const float vmax = row_vscale_max(rs, ctl->nv[s], lane);
+          shift = vmax > 0.0f ? log2f(vmax) : 0.0f;
+          inv_f = vmax > 0.0f ? 1.0f / vmax : 1.0f;
+#pragma unroll
+          for (int q = 0; q < 64; q += 4) {
+            const float4 k4 = reinterpret_cast<const float4*>(rs)[q >> 2];
+            x[q] = __float_as_uint(__uint_as_float(x[q]) * k4.x);
+            x[q + 1] = __float_as_uint(__uint_as_float(x[q + 1]) * k4.y);
+            x[q + 2] = __float_as_uint(__uint_as_float(x[q + 2]) * k4.z);
+            x[q + 3] = __float_as_uint(__uint_as_float(x[q + 3]) * k4.w);
+          }
+          // the row scales are used: this warp's share of releasing the stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
+        }
         const int kbase = p * kPage;
         const int lim = L + i_row;  // causal window: last visible key position of this row
         // a draft tree masks every page that holds window keys key by key:
@@ -1381,39 +1509,52 @@ size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms) {
 bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_pages, int num_sms) {
   const int Hkv = cache->num_kv_heads;
   const int R = W * (Hq / Hkv);
-  const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || (cache->dtype == SDVA_KV_FP8_E4M3 && encoder() != nullptr);
+  // the FP8 formats read their code tiles through tensor maps
+  const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || cache->dtype == SDVA_KV_INT8_G64 ||
+                        ((cache->dtype == SDVA_KV_FP8_E4M3 || cache->dtype == SDVA_KV_FP8_ROW) && encoder() != nullptr);
   // the partition's cost arithmetic is 32-bit (see Partition)
   const bool cost_ok = (long long)B * (max_pages + kUnitCost) * Hkv < (1LL << 31);
   return dtype_ok && cost_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 && num_sms <= kMaxSegments &&
          (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }
 
-int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream,
+// The split kernel for cache format KVT, in the mode the arguments select.
+template <int KVT>
+int launch_split_kvt(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream,
                      bool after_append) {
-  if (cache->dtype == SDVA_KV_INT4_G32) {
-    // the INT4 pools are read with 1-D bulk copies: no tensor maps
-    CUtensorMap none;
-    memset(&none, 0, sizeof(none));
-    auto kern = args.parent   ? verify_split_tc_kernel<SDVA_KV_INT4_G32, kModeTree>
-                : args.n_lane ? verify_split_tc_kernel<SDVA_KV_INT4_G32, kModeRagged>
-                              : verify_split_tc_kernel<SDVA_KV_INT4_G32, 0>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_INT4_G32>());
-    if (launch_split(kern, none, none, args, num_sms, smem_bytes<SDVA_KV_INT4_G32>(), stream, after_append) !=
-        cudaSuccess)
-      return SDVA_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if constexpr (Smem<KVT>::kDeq) {
+    // the INT4 and INT8 pools are read with 1-D bulk copies: no tensor maps
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
   } else {
-    CUtensorMap mk, mv;
     const long long rows = (long long)cache->num_pages * cache->num_kv_heads * kPage;
     if (!encode_pool_map(&mk, cache->k_codes, rows) || !encode_pool_map(&mv, cache->v_codes, rows))
       return SDVA_ERR_CUDA;
-    auto kern = args.parent   ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, kModeTree>
-                : args.n_lane ? verify_split_tc_kernel<SDVA_KV_FP8_E4M3, kModeRagged>
-                              : verify_split_tc_kernel<SDVA_KV_FP8_E4M3, 0>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<SDVA_KV_FP8_E4M3>());
-    if (launch_split(kern, mk, mv, args, num_sms, smem_bytes<SDVA_KV_FP8_E4M3>(), stream, after_append) !=
-        cudaSuccess)
-      return SDVA_ERR_CUDA;
   }
+  auto kern = args.parent   ? verify_split_tc_kernel<KVT, kModeTree>
+              : args.n_lane ? verify_split_tc_kernel<KVT, kModeRagged>
+                            : verify_split_tc_kernel<KVT, 0>;
+  // the shared-memory limit is a per-device attribute of the function: set it
+  // on every call, for the device current now
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<KVT>()) != cudaSuccess)
+    return SDVA_ERR_CUDA;
+  if (launch_split(kern, mk, mv, args, num_sms, smem_bytes<KVT>(), stream, after_append) != cudaSuccess)
+    return SDVA_ERR_CUDA;
+  return SDVA_OK;
+}
+
+int launch_verify_tc(const sdva_kv_cache* cache, const TcArgs& args, int num_sms, cudaStream_t stream,
+                     bool after_append) {
+  int rc;
+  switch (cache->dtype) {
+    case SDVA_KV_FP8_E4M3: rc = launch_split_kvt<SDVA_KV_FP8_E4M3>(cache, args, num_sms, stream, after_append); break;
+    case SDVA_KV_INT4_G32: rc = launch_split_kvt<SDVA_KV_INT4_G32>(cache, args, num_sms, stream, after_append); break;
+    case SDVA_KV_INT8_G64: rc = launch_split_kvt<SDVA_KV_INT8_G64>(cache, args, num_sms, stream, after_append); break;
+    case SDVA_KV_FP8_ROW: rc = launch_split_kvt<SDVA_KV_FP8_ROW>(cache, args, num_sms, stream, after_append); break;
+    default: return SDVA_ERR_UNSUPPORTED;
+  }
+  if (rc != SDVA_OK) return rc;
   if (cudaGetLastError() != cudaSuccess) return SDVA_ERR_CUDA;
   // A unit spans about num_sms / units + 1 CTAs: few -> one warp per row, many
   // -> one block of 8 warps per row.

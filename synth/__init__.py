@@ -36,6 +36,8 @@ PAGE = 64
 HEAD_DIM = 128
 KV_FP8 = 0
 KV_INT4 = 1
+KV_INT8 = 2
+KV_FP8_ROW = 3
 
 
 @dataclasses.dataclass(frozen=True)

@@ -103,6 +103,15 @@ def test_argument_validation_returns_before_cuda(lib):
     assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
     c.page_size, c.dtype = 64, 7
     assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
+    c.dtype = -1
+    assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -2
+    # every format's four cache arrays must be 16-byte aligned
+    for dt in range(4):
+        for field in ("k_codes", "v_codes", "k_scales", "v_scales"):
+            c.dtype = dt
+            setattr(c, field, P(0x1004))
+            assert app(ctypes.byref(c), fake, fake, 1, 1, fake, 1, fake, None, None) == -1, (dt, field)
+            setattr(c, field, fake)
     c.dtype = 0
     va = lib.verify_attn
     va.restype = ctypes.c_int
@@ -118,6 +127,12 @@ def test_argument_validation_returns_before_cuda(lib):
     odd = P(0x1008)
     assert va(ctypes.byref(c), odd, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
     assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, 0.088, odd, fake, 1 << 20, None, None) == -1
+    for dt in range(4):
+        c.dtype, c.v_scales = dt, P(0x1004)
+        assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -1
+    c.dtype, c.v_scales = 4, fake
+    assert va(ctypes.byref(c), fake, 4, 1, 4, fake, 1, fake, 10, 0.088, fake, fake, 1 << 20, None, None) == -2
+    c.dtype = 0
     sa = lib.spec_accept
     sa.restype = ctypes.c_int
     assert sa(fake, 1, 4, 100, None, fake, fake, None, None, None) == -1   # drafts needed when window > 1
@@ -159,6 +174,13 @@ def test_header_constants_match_the_binding(lib):
     assert int(defs["SDVA_STATUS_BAD_TREE"]) == sdva.STATUS_BAD_TREE
     assert int(defs["SDVA_STATUS_BAD_DRAFT"]) == sdva.STATUS_BAD_DRAFT
     assert int(defs["SDVA_ERR_WORKSPACE"]) == sdva.ERR_WORKSPACE
+    kinds = dict(re.findall(r"SDVA_KV_(\w+) = (\d+)", text))
+    assert {k: int(v) for k, v in kinds.items()} == {"FP8_E4M3": 0, "INT4_G32": 1, "INT8_G64": 2, "FP8_ROW": 3}
+    assert (sdva.KV_FP8_E4M3, sdva.KV_INT4_G32, sdva.KV_INT8_G64, sdva.KV_FP8_ROW) == (0, 1, 2, 3)
+    import oracle
+    import synth
+    assert (oracle.KV_FP8, oracle.KV_INT4, oracle.KV_INT8, oracle.KV_FP8_ROW) == (0, 1, 2, 3)
+    assert (synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW) == (0, 1, 2, 3)
     m = re.search(r"#define SDVA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
     assert m, "SDVA_NOALLOC_SCRATCH_BYTES not found"
     assert int(m.group(1)) << int(m.group(2)) == sdva.NOALLOC_SCRATCH_BYTES

@@ -1,7 +1,7 @@
 """GPU parity of kv_append_quant against the oracle: cache bytes and scales
-must be bit-exact (FP8 codes, fp32 page scales, INT4 nibbles, fp16 group
-scales), over exhaustive bf16 exponent bands, multi-step verify histories
-with scale growth, and the error paths."""
+must be bit-exact (FP8 codes, fp32 page scales, INT4 nibbles, INT8 codes,
+fp16 group scales, fp32 row scales), over exhaustive bf16 exponent bands,
+multi-step verify histories with scale growth, and the error paths."""
 import numpy as np
 import pytest
 import torch
@@ -12,6 +12,7 @@ from gpu_util import bf16_dev, cache_to_host, i32_dev
 
 pytestmark = pytest.mark.gpu
 PAGE = 64
+ALL_KV = [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW]
 
 
 def _sdva():
@@ -48,7 +49,7 @@ def _band_block(rng, e_top, shape):
     return rng.permutation(out).reshape(shape).astype(np.uint16)
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", ALL_KV)
 def test_exhaustive_bf16_bands(dtype):
     sdva = _sdva()
     Hkv = 4
@@ -74,7 +75,7 @@ def test_exhaustive_bf16_bands(dtype):
     _assert_cache_equal(gcache, ocache, "bands")
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", ALL_KV)
 def test_growth_reencode_bands(dtype):
     """Half a page at a small scale, then the other half at scales up to 2^40
     larger: every earlier code is re-encoded (FP8)."""
@@ -99,7 +100,7 @@ def test_growth_reencode_bands(dtype):
     _assert_cache_equal(gcache, ocache, "growth")
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", ALL_KV)
 @pytest.mark.parametrize("W", [1, 5, 16])
 def test_verify_history_bit_exact(dtype, W):
     """Many verify steps with random accept lengths (rejected slots are
@@ -166,7 +167,7 @@ def test_host_argument_errors():
 
 # ---- per-lane token counts -------------------------------------------------
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", ALL_KV)
 def test_ragged_append_history_parity(dtype):
     sdva = _sdva()
     rng = np.random.default_rng(77 + dtype)

@@ -19,7 +19,7 @@ def _sdva():
     return sdva, VerifyStep
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW])
 def test_multi_step_loop_matches_oracle(dtype):
     sdva, VerifyStep = _sdva()
     W, Hq, Hkv, V = 6, 12, 2, 3000
@@ -55,7 +55,7 @@ def test_multi_step_loop_matches_oracle(dtype):
     assert np.array_equal(g["k_codes"], ocache.k_codes) and np.array_equal(g["v_codes"], ocache.v_codes)
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW])
 def test_ragged_step_loop_matches_oracle(dtype):
     """Lanes with their own draft counts d_b in one padded window: the ragged
     append writes 1 + d_b tokens per lane, verify rows 0 .. d_b are compared,
@@ -182,7 +182,7 @@ def test_checkpoint_restore_continues_identically():
         assert torch.equal(o1, o2) and torch.equal(a1, a2)
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW])
 def test_verify_step_equals_the_three_calls(dtype):
     """verify_step (the chained launch) leaves the same cache bytes, attention
     rows, accept lengths, tokens, committed lengths and status as

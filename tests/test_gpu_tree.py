@@ -122,10 +122,13 @@ TREE_CASES = [
     (0, [0, 64, 4097], 7, 8, 1),
     (1, [0, 129, 900], 8, 24, 4),
     (1, [700, 31], 16, 8, 1),
+    (2, [0, 129, 900], 8, 24, 4),
+    (3, [5, 200, 1500, 63], 16, 24, 4),
 ]
+KV_NAMES = {0: "fp8", 1: "int4", 2: "int8", 3: "fp8row"}
 
 
-@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"{'fp8' if c[0] == 0 else 'int4'}-W{c[2]}-{c[3]}q{c[4]}kv")
+@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"{KV_NAMES[c[0]]}-W{c[2]}-{c[3]}q{c[4]}kv")
 def test_tree_attention_random_trees(case):
     """Every element of every row within |g - r| <= 2e-3 + 1e-2 |r| of the
     oracle's fp64 ancestor-masked attention, on random trees."""
@@ -144,7 +147,7 @@ def test_tree_attention_random_trees(case):
     assert_close(got, want, f"tree {case}")
 
 
-@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("dtype", [0, 1, 2, 3])
 def test_chain_tree_equals_causal_verify(dtype):
     """A chain tree (parent i - 1) is the causal window: bit-identical to verify_attn."""
     import synth

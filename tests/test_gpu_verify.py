@@ -1,6 +1,6 @@
 """GPU parity of verify_attn against the oracle (fp64): every output element
 within |g - r| <= 2e-3 + 1e-2 |r| on small cases spanning several pages,
-splits and ragged tails, FP8 and INT4; on the five full-size workloads in
+splits and ragged tails, in all four cache formats; on the five full-size workloads in
 the benchmark's launch configuration, the KV bytes of two lanes bit for bit,
 every row of one lane and sampled rows of another; plus GPU-side invariants
 (page-table permutation, split count, invalid lanes)."""
@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import SM_SCALE, assert_close, bf16_dev, both_fraction, fill_both, i32_dev, lane_pages
+from gpu_util import KV_NAMES, SM_SCALE, assert_close, bf16_dev, both_fraction, fill_both, i32_dev, lane_pages
 
 pytestmark = pytest.mark.gpu
 
@@ -50,10 +50,19 @@ SMALL = [
     # several CTAs; some CTAs' cost shares fall inside a unit's start cost
     (synth.KV_FP8, [(37 * i) % 300 for i in range(40)], 16, 24, 4),
     (synth.KV_INT4, [(53 * i) % 400 for i in range(24)], 8, 24, 4),
+    # INT8 group-64 and FP8 row scales (at most 128 rows per kv head)
+    (synth.KV_INT8, [0, 64, 129, 900], 8, 24, 4),
+    (synth.KV_INT8, [1200, 77], 16, 12, 2),
+    (synth.KV_INT8, [700], 1, 4, 1),
+    (synth.KV_INT8, [(53 * i) % 400 for i in range(24)], 8, 24, 4),
+    (synth.KV_FP8_ROW, [0, 1, 63, 64, 65, 700], 1, 4, 1),
+    (synth.KV_FP8_ROW, [130, 4097, 31], 16, 24, 4),
+    (synth.KV_FP8_ROW, [333, 64], 16, 8, 1),
+    (synth.KV_FP8_ROW, [(37 * i) % 300 for i in range(40)], 16, 24, 4),
 ]
 
 
-@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{'fp8' if c[0] == 0 else 'int4'}-W{c[2]}-{c[3]}q{c[4]}kv")
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{KV_NAMES[c[0]]}-W{c[2]}-{c[3]}q{c[4]}kv")
 def test_small_cases_all_elements(case):
     dtype, lens, W, Hq, Hkv = case
     spec = synth.Spec("small", 17 + W, len(lens), 0, 0, Hq, Hkv, W, dtype, None, 0.7, True)
