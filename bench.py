@@ -567,6 +567,44 @@ def run_gpu(args):
                    "timing": "CUDA events around the call after an L2 flush, same steps and warm-up as the main loop"}
         del qd
 
+    # ---- the attention's other modes on the same workload: per-lane row counts, a draft tree ----
+    modes = None
+    if not args.no_all_workloads:
+        rng = np.random.default_rng(11)
+        counts = rng.integers(1, W + 1, size=B).astype(np.int32)
+        parent = np.zeros((B, W), np.int32)
+        for i in range(1, W):
+            parent[:, i] = rng.integers(0, i, size=B)
+        n_dev = torch.from_numpy(counts).to(dev)
+        full_dev = torch.full((B,), W, dtype=torch.int32, device=dev)
+        par_dev = torch.from_numpy(parent).to(dev)
+        mc = spec.ctx_hi
+
+        def timed(call):
+            def fn(e):
+                if e:
+                    e[0].record(stream)
+                call()
+                if e:
+                    e[1].record(stream)
+            evs = time_loop(fn, args.steps, args.warmup, flush_l2)
+            return 1e3 * float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+        ws = vs.workspace
+        t_causal = timed(lambda: sdva.verify_attn(wl.cache, wl.q, wl.table, wl.seq, mc, float(SM_SCALE), vs.out, ws,
+                                                  vs.status))
+        t_full = timed(lambda: sdva.verify_attn_ragged(wl.cache, wl.q, full_dev, wl.table, wl.seq, mc, float(SM_SCALE),
+                                                       vs.out, ws, vs.status))
+        t_rag = timed(lambda: sdva.verify_attn_ragged(wl.cache, wl.q, n_dev, wl.table, wl.seq, mc, float(SM_SCALE),
+                                                      vs.out, ws, vs.status))
+        t_tree = timed(lambda: sdva.verify_attn_tree(wl.cache, wl.q, par_dev, wl.table, wl.seq, mc, float(SM_SCALE),
+                                                     vs.out, ws, vs.status))
+        assert int(vs.status.item()) == 0, sdva.sdva_status_string(int(vs.status.item()))
+        modes = {"verify_attn_us": t_causal, "verify_attn_ragged_full_counts_us": t_full,
+                 "verify_attn_ragged_us": t_rag, "ragged_counts": [int(c) for c in counts],
+                 "ragged_rows_fraction": float(counts.sum()) / (B * W), "verify_attn_tree_us": t_tree,
+                 "tree": "random: slot i hangs under a uniform earlier slot (seed 11)",
+                 "timing": "CUDA events around the call after an L2 flush, same steps and warm-up as the main loop"}
+
     # ---- e2e: host buffers through the public API ----
     q, kw, vw, seq, table, cache = wl.q, wl.kw, wl.vw, wl.seq, wl.table, wl.cache
     host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("kw", kw), ("vw", vw))}
@@ -675,6 +713,7 @@ def run_gpu(args):
         "all_workloads": all_workloads,
         "spec_accept_lazy": lazy,
         "spec_accept_sampled": sampled,
+        "verify_modes": modes,
         "gpu_launches": args.steps * wl.launches_per_step(),
         "clocks": clocks,
         "wall_s_timed_loop": wall,

@@ -1,13 +1,17 @@
 """GPU parity of spec_accept_sampled (lossless stochastic acceptance) against
-the oracle.  The kernel decides in fp32 with hardware exp2, the oracle in
-fp64, so a decision whose uniform lies within rounding of its boundary may
-go either way: every lane is run through the oracle three times, with both
-uniforms as given and scaled by (1 - 1e-4) and (1 + 1e-4).  Accept lengths
-and accepted drafts must match exactly where the three runs agree; the drawn
-token must lie between the draws at the two scaled uniforms (a window of
-1e-4 of the probability mass), which is exact where they agree.  The
-distribution of the GPU's own draws is also checked against the target
-(chi-square), independently of the oracle."""
+the oracle.  The kernel decides in fp32 with the hardware exp2, the oracle in
+fp64.  The test bounds the kernel's fp32 error from its arithmetic (see
+_eps_row) and checks each decision against the fp64 value with that bound:
+- a ratio test u q < p whose fp64 margin exceeds the bound must come out as
+  in fp64; the lanes where one sits inside it ("straddle" lanes) are counted
+  and reported, and their accept length must be one the bound allows;
+- the drawn token's cumulative-mass interval must hold the fp64 target
+  u_sample Z to within the bound; the token must equal the fp64 draw on at
+  least a stated share of the lanes.
+The fp64 reference values (softmax, cumulative residual mass) are checked
+against the oracle's own decisions at the exact uniforms.  The distribution
+of the GPU's draws is also checked against the target (chi-square),
+independently of the oracle."""
 import math
 
 import numpy as np
@@ -18,7 +22,51 @@ import oracle
 from gpu_util import i32_dev
 
 pytestmark = pytest.mark.gpu
-DELTA = 1e-4
+U = 2.0 ** -24  # fp32 unit roundoff
+# bound assumed for the relative error of the hardware exp2 (ex2.approx.ftz.f32)
+E = 2.0 ** -21
+LN2 = math.log(2.0)
+LOG2E = 1.0 / LN2
+
+
+def _stats_parts(rows):
+    """CTAs per logits row of the statistics kernel, chosen as the host does:
+    enough to cover every SM about four times, at most one 8-CTA cluster."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    parts = 1
+    while parts < 8 and rows * parts < 4 * sms:
+        parts *= 2
+    return parts
+
+
+def _eps_row(lrow, parts):
+    """Relative error bound of the kernel's p(x) = exp2((l_x - M) log2e) / S
+    over one fp32 logits row.  S is summed per thread in groups of four
+    (each group: one rescale of the partial by exp2 and four additions), then
+    combined over 5 warp levels, 7 sequential warp partials and parts - 1
+    cluster partials (each a rescale and an addition).  Along any path to S:
+    at most 1 + levels exp2 evaluations (E each), 3 + 2 levels roundings (U
+    each), and an exp2 argument error of 3U |arg| per evaluation, where the
+    arguments of one path's rescales add up to at most the row's range R (the
+    running max only grows) and the element's own argument is bounded in the
+    weighted mean.  p adds its own exp2 (E + 3U |arg|) and the division (U).
+    Returns (eps for the element with argument a, as a function; the bound
+    at the row's largest argument)."""
+    V = lrow.size
+    x = lrow.astype(np.float64)
+    M = x.max()
+    arg = (M - x) * LOG2E
+    w = np.exp2(-arg)
+    abar = float((w * arg).sum() / w.sum())
+    R = float(arg.max())
+    chunk = (((V + parts - 1) // parts) + 3) & ~3
+    g = -(-chunk // 1024)
+    levels = g + 5 + 7 + (parts - 1)
+    eps_s = E * (1 + levels) + U * (3 + 2 * levels) + 3 * U * LN2 * (abar + R)
+
+    def eps(a):
+        return eps_s + E + 3 * U * LN2 * a + U
+    return eps, eps(R)
 
 
 def _inputs(seed, B, W, V, sharp=2.0):
@@ -59,35 +107,76 @@ def _run(logits, q, drafts, ua, us, seq_lens=None, offset=0):
     return acc.cpu().numpy(), tok.cpu().numpy(), None if sl is None else sl.cpu().numpy(), int(st.item())
 
 
+def _softmax64(l):
+    x = l.astype(np.float64)
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
 def _check(logits, q, drafts, ua, us, got, seq_lens=None):
-    """The accept length must be the oracle's wherever that is robust to the
-    uniforms' rounding (else one of the nearby lengths).  Given it, the
-    accepted drafts and the -1 tail are exact, and the drawn token lies
-    between the oracle's draws at u_sample * (1 - 1e-4) and * (1 + 1e-4)
-    (the inverse CDF is monotone in the uniform): exact where they agree.
-    Returns the number of lanes checked exactly."""
-    one = np.float32(np.nextafter(np.float32(1), np.float32(0)))
-    runs = [oracle.spec_accept_sampled(logits, q, drafts, np.minimum(ua * f, one).astype(np.float32),
-                                       np.minimum(us * f, one).astype(np.float32), seq_lens)
-            for f in (1.0, 1.0 - DELTA, 1.0 + DELTA)]
-    assert got[3] == runs[0][3]
-    W = logits.shape[1]
-    exact = 0
-    for b in range(logits.shape[0]):
+    """Checks one GPU run (see the module docstring).  Returns (lanes whose
+    token equals the fp64 draw, straddle lanes, largest cumulative-mass miss
+    of a draw, the largest bound allowed for it)."""
+    B, W, V = logits.shape
+    d = W - 1
+    parts = _stats_parts(B * W)
+    orc = oracle.spec_accept_sampled(logits, q, drafts, ua, us, seq_lens)
+    assert got[3] == orc[3]
+    n_tiles = -(-V // 1024)
+    slices = min(64, max(1, -(-V // 4096)))
+    exact = straddle = 0
+    worst_miss = worst_eta = 0.0
+    for b in range(B):
+        P = _softmax64(logits[b])
+        possible = []
+        for i in range(d):
+            x = int(drafts[b, i])
+            if x < 0 or x >= V:
+                possible.append(i)
+                break
+            eps, _ = _eps_row(logits[b, i], parts)
+            px = P[i, x]
+            margin = (px - float(ua[b, i]) * float(q[b, i, x])) / px
+            tol = eps((logits[b, i].astype(np.float64).max() - float(logits[b, i, x])) * LOG2E) + 2 * U
+            if margin > tol:
+                continue
+            possible.append(i)
+            if margin < -tol:
+                break  # a clear rejection
+            # inside the bound: either outcome is allowed; continue as accepted
+        else:
+            possible.append(d)
         a = int(got[0][b])
-        lens = {int(r[0][b]) for r in runs}
-        assert a in lens, (b, a, lens)
-        if len(lens) > 1:
-            continue  # the accept decision itself sits on its boundary
+        assert a in possible, (b, a, possible)
+        straddle += len(possible) > 1
+        assert int(orc[0][b]) in possible, (b, int(orc[0][b]), possible)
         tok = got[1][b]
         assert list(tok[:a]) == list(drafts[b, :a]) and (tok[a + 1:] == -1).all(), (b, tok)
-        ks = [int(r[1][b][a]) for r in runs]
-        lo, hi = min(ks), max(ks)
-        assert lo <= tok[a] <= hi, (b, int(tok[a]), ks)
-        exact += lo == hi
+        # the draw from row a: the residual max(0, p - q), or p after a full acceptance
+        w = np.maximum(0.0, P[a] - q[b, a].astype(np.float64)) if a < d else P[a]
+        if not w.sum() > 0.0:
+            w = P[a]
+        C = np.cumsum(w)
+        Z = C[-1]
+        T = float(us[b]) * Z
+        k_ref = min(int(np.searchsorted(C, T, side="right")), int(np.nonzero(w > 0)[0][-1]))
+        if int(orc[0][b]) == a:  # the fp64 reference agrees with the oracle's own draw
+            assert int(orc[1][b][a]) == k_ref, (b, int(orc[1][b][a]), k_ref)
+        k = int(tok[a])
+        lo_c = C[k - 1] if k > 0 else 0.0
+        hi_c = C[k]
+        miss = 0.0 if lo_c <= T < hi_c else (lo_c - T if T < lo_c else T - hi_c)
+        _, eps_p = _eps_row(logits[b, a], parts)
+        # cumulative and total mass: the weights' error (eps_p of a mass <= 1),
+        # the sums (4-term, 1024-logit block scan, tiles of a slice, slices),
+        # and the target's product
+        eta = 2.0 * (eps_p + U * (2 + 13 + n_tiles + slices)) + U
+        assert miss <= eta, (b, k, k_ref, miss, eta)
+        worst_miss, worst_eta = max(worst_miss, miss), max(worst_eta, eta)
+        exact += k == k_ref
         if seq_lens is not None:
             assert got[2][b] == seq_lens[b] + 1 + a
-    return exact
+    return exact, straddle, worst_miss, worst_eta
 
 
 @pytest.mark.parametrize("B,W,V,offset", [(8, 16, 151936, 0), (12, 8, 151936, 0), (8, 16, 151936, 1),
@@ -96,9 +185,13 @@ def test_sampled_parity(B, W, V, offset):
     logits, q, drafts, ua, us = _inputs(60 + B + W, B, W, V)
     L = np.arange(B, dtype=np.int32) * 10
     got = _run(logits, q, drafts, ua, us, L, offset)
-    exact = _check(logits, q, drafts, ua, us, got, L)
-    if V <= 5000:  # wide bins: nearly every draw is pinned exactly
-        assert exact >= B - 1, exact
+    exact, straddle, miss, eta = _check(logits, q, drafts, ua, us, got, L)
+    print(f"B={B} W={W} V={V}: {exact}/{B} draws equal the fp64 draw, {straddle} straddle lanes, "
+          f"largest mass miss {miss:.3g} (bound {eta:.3g})")
+    assert straddle <= 1, straddle
+    # the fp32 error (measured far below the bound) moves a draw only when the
+    # target sits that close to a token boundary
+    assert exact >= B - (1 if V <= 5000 else 2), exact
     assert (got[0] >= 0).all() and (got[0] <= W - 1).all()
 
 
@@ -109,9 +202,9 @@ def test_sampled_window_of_one_and_peaked_rows():
     logits[:, 0, 17] = 14.0  # most of the mass (about 0.83) on one token
     us = rng.random(B).astype(np.float32)
     got = _run(logits, None, np.zeros((B, 0), np.int32), np.zeros((B, 0), np.float32), us)
-    exact = _check(logits, np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
-                   np.zeros((B, 0), np.float32), us, got)
-    assert (got[0] == 0).all() and exact >= B // 2  # token 17 holds most of the mass: its draws are exact
+    exact, straddle, _, _ = _check(logits, np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
+                                   np.zeros((B, 0), np.float32), us, got)
+    assert (got[0] == 0).all() and straddle == 0 and exact >= B - 2
 
 
 def test_sampled_bad_drafts_and_zero_draft_probability():

@@ -18,7 +18,7 @@ from gpu_util import SM_SCALE, assert_close, bf16_dev, fill_both, i32_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW])
 def test_wait_that_runs_out_is_reported_and_recovered(dtype):
     import speculative_decode_verify_append_gb300 as sdva
     lens, W = [3000, 700, 12000, 64], 8
