@@ -59,8 +59,9 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "5119446dc563f5658948904fcdc2e192199192b2615caf0993d71fd444642c8e",
-               "bytes": {"multi_lane": 314576128, "long_context": 249101824}}
+NCU_TRAFFIC = {"sources_sha256": "3e237b1088087cbe15e024e94abddba7149c55246d5fdb580e043eba842ee6dc",
+               "bytes": {"multi_lane": 314627840, "long_context": 249112576, "int4_12slot": 338141440,
+                         "multi_lane_int8": 323842048, "multi_lane_fp8row": 323811328}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
@@ -317,7 +318,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    spec = synth.WORKLOADS[args.workload]
+    spec = all_workload_specs()[args.workload]
     step = synth.make_step(spec)
     B = len(step.seq_lens)
     lanes = list(range(B))
@@ -453,7 +454,7 @@ def run_gpu(args):
         clean.amax()
     stream = torch.cuda.current_stream()
 
-    spec = synth.WORKLOADS[args.workload]
+    spec = all_workload_specs()[args.workload]
     wl = GpuWorkload(spec, dev)
     step, vs = wl.step, wl.vs
     B, W, Hq = step.q.shape[:3]
@@ -681,7 +682,8 @@ def run_gpu(args):
             sep_us = 1e3 * float(np.mean([e[0].elapsed_time(e[3]) for e in e_sep]))
             gbs = w.alg / (v_us / 1e6) / 1e9
             all_workloads[name] = {"verify_attn_us": v_us, "verify_attn_gbs": gbs, "frac": gbs / peak,
-                                   "algorithmic_bytes": w.alg, "step_us": st_us, "steps_per_s": 1e6 / st_us,
+                                   "algorithmic_bytes": w.alg, "traffic": ncu_traffic(name),
+                                   "step_us": st_us, "steps_per_s": 1e6 / st_us,
                                    "separate_calls_step_us": sep_us, "kv": KV_LABELS[w.spec.kv_dtype]}
             if w is not wl:
                 del w
@@ -790,7 +792,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workload_specs()))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-workloads", action="store_true",
