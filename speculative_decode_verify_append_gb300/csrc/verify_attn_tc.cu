@@ -861,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         if constexpr (kRow) {
           nv = ctl->nv[s];
           const float vmax = row_vscale_max(rs, nv, lane);
-          inv_max = vmax > 0.0f ? 1.0f / vmax : 0.0f;
+          inv_max = vmax > 0.0f ? __fdividef(1.0f, vmax) : 0.0f;
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1016,15 +1016,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
           // divided it out of the fp16 V)
           const float* rs = reinterpret_cast<const float*>(base_ptr + SM::kOffRowSc + s * kRowScaleBytes);
           const float vmax = row_vscale_max(rs, ctl->nv[s], lane);
-          shift = vmax > 0.0f ? log2f(vmax) : 0.0f;
-          inv_f = vmax > 0.0f ? 1.0f / vmax : 1.0f;
+          shift = vmax > 0.0f ? __log2f(vmax) : 0.0f;
+          inv_f = vmax > 0.0f ? __fdividef(1.0f, vmax) : 1.0f;
 #pragma unroll
           for (int q = 0; q < 64; q += 4) {
             const float4 k4 = reinterpret_cast<const float4*>(rs)[q >> 2];
-            x[q] = __float_as_uint(__uint_as_float(x[q]) * k4.x);
-            x[q + 1] = __float_as_uint(__uint_as_float(x[q + 1]) * k4.y);
-            x[q + 2] = __float_as_uint(__uint_as_float(x[q + 2]) * k4.z);
-            x[q + 3] = __float_as_uint(__uint_as_float(x[q + 3]) * k4.w);
+            const float2 a = f2_unpack(fmul2(f2_pack(__uint_as_float(x[q]), __uint_as_float(x[q + 1])), f2_pack(k4.x, k4.y)));
+            const float2 b = f2_unpack(fmul2(f2_pack(__uint_as_float(x[q + 2]), __uint_as_float(x[q + 3])), f2_pack(k4.z, k4.w)));
+            x[q] = __float_as_uint(a.x);
+            x[q + 1] = __float_as_uint(a.y);
+            x[q + 2] = __float_as_uint(b.x);
+            x[q + 3] = __float_as_uint(b.y);
           }
           // the row scales are used: this warp's share of releasing the stage
           __syncwarp();
