@@ -13,7 +13,8 @@ One JSON line (rank 0):
                fraction of the measured copy bandwidth (roofline object)
   e2e          the same steps/s through the C ABI from pinned HOST buffers,
                host->device inputs and device->host results inside the timing
-               (the logits copy overlaps append and verify: only accept reads it)
+               (the logits copy overlaps append and verify: only accept reads it,
+               lane chunk by lane chunk as the chunks land)
   cpu_baseline the CPU oracle on the host cores, on a bounded sample
   spec_accept_lazy  the acceptance that reads each lane's logits rows only up
                to its first disagreement (timed apart, after the main loop),
@@ -622,38 +623,61 @@ def run_gpu(args):
     e2e_steps = max(10, min(args.steps, 200))
     e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
     # The logits (most of a step's input bytes) are read only by spec_accept:
-    # their copy runs in two halves on two side streams, beside append and
-    # verify, and accept waits for it.  Each step's copies start inside its
-    # timed region (the side streams wait for everything issued before it).
-    side = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    # they are copied in two lane chunks on one side stream while append and
+    # verify run, and each chunk's acceptance runs as soon as that chunk has
+    # landed (lanes are independent), so only the last chunk's acceptance
+    # follows the copy.  The attention output is read back on a second side
+    # stream once verify_attn is done.  (The host link carried ~209 GB/s on
+    # this part whether one copy, several concurrent copies or a kernel read
+    # the pinned buffer.)  The step -- every copy and every call -- is captured
+    # once in a CUDA graph and replayed each step, as a serving loop does: the
+    # Python launch overhead of ~30 calls per step would otherwise leave the
+    # GPU idle between them.
+    cs = torch.cuda.Stream(device=dev)  # host -> device: logits
+    ds = torch.cuda.Stream(device=dev)  # device -> host: attention output
+    n_chunks = min(B, 2) if logits is not None else 0
+    bounds = [(B * i // n_chunks, B * (i + 1) // n_chunks) for i in range(n_chunks)]
+
+    def e2e_body():
+        cur = torch.cuda.current_stream()
+        ready = []
+        # the small inputs first, so that append and verify do not wait behind the logits on the copy engine
+        for n, t in host_in.items():
+            if n != "logits":
+                dev_in[n].copy_(t, non_blocking=True)
+        if logits is not None:
+            cs.wait_stream(cur)  # the previous step's acceptance has read the old logits
+            with torch.cuda.stream(cs):
+                for lo, hi in bounds:
+                    dev_in["logits"][lo:hi].copy_(host_in["logits"][lo:hi], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    ready.append(ev)
+        vs.append(cache, kw, vw, table, seq)
+        vs.attend(cache, q, table, seq)
+        ds.wait_stream(cur)
+        with torch.cuda.stream(ds):
+            host_out["out"].copy_(vs.out, non_blocking=True)
+        if logits is not None:
+            for (lo, hi), ev in zip(bounds, ready):
+                cur.wait_event(ev)
+                sdva.spec_accept(logits[lo:hi], drafts[lo:hi], vs.accept_len[lo:hi], vs.out_tokens[lo:hi],
+                                 wl.commit_lens[lo:hi], vs.status)
+            host_out["acc"].copy_(vs.accept_len, non_blocking=True)
+            host_out["tok"].copy_(vs.out_tokens, non_blocking=True)
+        cur.wait_stream(ds)
+
+    e2e_body()  # eager once (the library sets its per-device attributes outside the capture)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        e2e_body()
+    torch.cuda.synchronize()
     for k in range(e2e_steps + 3):
         flush_l2()
         if k >= 3:
             e_ev[k - 3][0].record(stream)
-        logits_ready = []
-        if logits is not None:
-            half = logits.shape[0] // 2 if logits.shape[0] > 1 else logits.shape[0]
-            parts = [(0, half), (half, logits.shape[0])] if half < logits.shape[0] else [(0, logits.shape[0])]
-            for (lo, hi), cs in zip(parts, side):
-                cs.wait_stream(stream)  # the previous step's accept has read the old logits
-                with torch.cuda.stream(cs):
-                    dev_in["logits"][lo:hi].copy_(host_in["logits"][lo:hi], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(cs)
-                logits_ready.append(ev)
-        for n, t in host_in.items():
-            if n != "logits":
-                dev_in[n].copy_(t, non_blocking=True)
-        vs.append(cache, kw, vw, table, seq)
-        vs.attend(cache, q, table, seq)
-        if logits is not None:
-            for ev in logits_ready:
-                stream.wait_event(ev)
-            vs.accept(logits, drafts, wl.commit_lens)
-        host_out["out"].copy_(vs.out, non_blocking=True)
-        if logits is not None:
-            host_out["acc"].copy_(vs.accept_len, non_blocking=True)
-            host_out["tok"].copy_(vs.out_tokens, non_blocking=True)
+        graph.replay()
         if k >= 3:
             e_ev[k - 3][1].record(stream)
     torch.cuda.synchronize()
@@ -710,8 +734,10 @@ def run_gpu(args):
                      "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "algorithmic_bytes": alg},
         "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "calls": "kv_append_quant, verify_attn, spec_accept from pinned host buffers (the logits copy "
-                         "overlaps append and verify)"},
+                "calls": "kv_append_quant, verify_attn, spec_accept and every host<->device copy of the step, "
+                         "from pinned host buffers, captured once in a CUDA graph and replayed each step (the "
+                         "logits copied in two lane chunks under append and verify, each chunk accepted as it "
+                         "lands)"},
         "all_workloads": all_workloads,
         "spec_accept_lazy": lazy,
         "spec_accept_sampled": sampled,
