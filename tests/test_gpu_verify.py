@@ -89,14 +89,26 @@ def _assert_lane_pages_equal(gcache, ocache, step, lanes, what):
             assert diff.size == 0, f"{what} lane {b} {n}: {len(diff)} differing entries, first {diff[:5].tolist()}"
 
 
-@pytest.mark.parametrize("name", ["tiny", "plain_decode", "multi_lane", "long_context", "int4_12slot"])
+def _workload(name):
+    """The five workloads, and the 8-lane one with its cache in the INT8
+    group-64 or FP8 row-scale format (same seed, lengths and shapes)."""
+    import dataclasses
+    for tag, dt in (("_int8", synth.KV_INT8), ("_fp8row", synth.KV_FP8_ROW)):
+        if name.endswith(tag):
+            base = name[: -len(tag)]
+            return dataclasses.replace(synth.WORKLOADS[base], name=name, kv_dtype=dt)
+    return synth.WORKLOADS[name]
+
+
+@pytest.mark.parametrize("name", ["tiny", "plain_decode", "multi_lane", "long_context", "int4_12slot",
+                                  "multi_lane_int8", "multi_lane_fp8row"])
 def test_full_workload(name):
     """At the workload's full size and in the benchmark's launch configuration
     (max_context = the workload's upper context bound): the KV bytes (codes and
     scales) of two lanes' pages bit for bit after the context fill and the
     window append, every row of one lane element by element, and sampled rows
     of the other lane.  Reports max-abs and max-rel over the compared rows."""
-    spec = synth.WORKLOADS[name]
+    spec = _workload(name)
     step = synth.make_step(spec, with_accept=False)
     B, W, Hq = step.q.shape[:3]
     rng = np.random.default_rng(5)
