@@ -393,19 +393,20 @@ __device__ __forceinline__ void store_q_row_smem(const uint16_t* qrow, int e, ui
 __device__ __forceinline__ void int4_group_to_f16(uint4 codes, uint32_t scale_bits, uint4 (&out)[4]) {
   const __half2 s2 = __halves2half2(__ushort_as_half((unsigned short)scale_bits),
                                     __ushort_as_half((unsigned short)scale_bits));
+  // nibble n with its sign bit flipped is the byte q + 8; placed under the
+  // fp16 exponent of 1024 (0x64 high byte) it reads 1032 + q, exactly
   const __half2 bias = __floats2half2_rn(1032.0f, 1032.0f);
   const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t lo = cw[k] & 0x0F0F0F0Fu, hi = (cw[k] >> 4) & 0x0F0F0F0Fu;
+    const uint32_t lo = (cw[k] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((cw[k] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
     const uint32_t d03 = __byte_perm(lo, hi, 0x5140);  // bytes: dims 0, 1, 2, 3 of this word
     const uint32_t d47 = __byte_perm(lo, hi, 0x7362);  // dims 4, 5, 6, 7
     uint32_t h[4];
     const uint32_t src[2] = {d03, d47};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t spread = __byte_perm(src[q >> 1], 0u, (q & 1) ? 0x4342 : 0x4140);  // two dims, 16 bits each
-      const uint32_t biased = (spread | 0x64006400u) ^ 0x00080008u;
+      const uint32_t biased = __byte_perm(src[q >> 1], 0x64646464u, (q & 1) ? 0x4342 : 0x4140);  // two dims
       __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&biased), bias);
       v = __hmul2(v, s2);
       h[q] = *reinterpret_cast<const uint32_t*>(&v);
