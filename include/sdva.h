@@ -208,8 +208,12 @@ size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, in
  * and V are widened to fp16 (code * scale, one rounding); FP8-row V is
  * widened to fp16 as code * (s_j / s_max), s_max the largest V row scale of
  * the page's written rows, so a row whose scale is below 2^-14 s_max keeps
- * fewer significant bits (fp16 subnormals).  INT8 and FP8-row need at most
- * 128 rows per kv head (window * Hq / Hkv <= 128; else SDVA_ERR_UNSUPPORTED).
+ * fewer significant bits (fp16 subnormals).  INT8 and FP8-row are served by
+ * the tensor-core kernels only, which need at most 128 rows per kv head
+ * (window * Hq / Hkv <= 128), at most 1024 lanes, num_pages * num_kv_heads *
+ * 64 < 2^31 and num_lanes * (max_pages_per_lane + 16) * num_kv_heads < 2^31
+ * (else SDVA_ERR_UNSUPPORTED; FP8 and INT4 calls outside these limits run on
+ * the CUDA-core / mma.sync kernels, causal window only).
  * Returns SDVA_OK or a negative SDVA_ERR_*.
  */
 int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
