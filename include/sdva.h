@@ -213,7 +213,7 @@ size_t verify_attn_workspace_size(int num_lanes, int window, int num_q_heads, in
  * (window * Hq / Hkv <= 128), at most 1024 lanes, num_pages * num_kv_heads *
  * 64 < 2^31 and num_lanes * (max_pages_per_lane + 16) * num_kv_heads < 2^31
  * (else SDVA_ERR_UNSUPPORTED; FP8 and INT4 calls outside these limits run on
- * the CUDA-core / mma.sync kernels, causal window only).
+ * the mma.sync kernels, causal window only).
  * Returns SDVA_OK or a negative SDVA_ERR_*.
  */
 int verify_attn(const sdva_kv_cache* cache, const void* q, int num_q_heads, int num_lanes, int window,
