@@ -60,9 +60,9 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "3e237b1088087cbe15e024e94abddba7149c55246d5fdb580e043eba842ee6dc",
-               "bytes": {"multi_lane": 314627840, "long_context": 249112576, "int4_12slot": 338141440,
-                         "multi_lane_int8": 323842048, "multi_lane_fp8row": 323811328}}
+NCU_TRAFFIC = {"sources_sha256": "6eceb5dd8a7aa6fc7710bc865b3cf6ff9df4788b7fbf22e621f62feb1525ca19",
+               "bytes": {"multi_lane": 314599680, "long_context": 249038848, "int4_12slot": 338024448,
+                         "multi_lane_int8": 323879168, "multi_lane_fp8row": 324170240}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
