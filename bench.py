@@ -58,20 +58,28 @@ METRIC = "verify_attn HBM GB/s (% of GB300 peak) and verify steps/s at 8 lanes"
 DEFAULT_WORKLOAD = "multi_lane"
 # dram bytes (read + write) of one verify_attn call (split + merge kernels),
 # from an ncu capture of the kernels built from sources with this SHA-256
-# (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order);
+# (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order, comments stripped);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "6eceb5dd8a7aa6fc7710bc865b3cf6ff9df4788b7fbf22e621f62feb1525ca19",
+NCU_TRAFFIC = {"sources_sha256": "f7074bccaab392bef674ed63b44a2a5b668334679699e331f3b4aa10ffd5c8b3",
                "bytes": {"multi_lane": 314599680, "long_context": 249038848, "int4_12slot": 338024448,
                          "multi_lane_int8": 323879168, "multi_lane_fp8row": 324170240}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
+
+
+def code_of(text: str) -> str:
+    """A source file without its // comments, trailing blanks and empty lines:
+    what the counters depend on (the files hold no block comments and no //
+    inside string literals)."""
+    lines = (ln.split("//", 1)[0].rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
 
 
 def kernel_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     for n in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "speculative_decode_verify_append_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "speculative_decode_verify_append_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()
 
 

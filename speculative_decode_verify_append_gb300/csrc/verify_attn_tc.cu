@@ -1,4 +1,5 @@
-// verify_attn_tc.cu -- verify attention over the FP8 E4M3 paged cache on the
+// verify_attn_tc.cu -- verify attention over the paged, quantised cache (FP8
+// E4M3 with page or row scales, INT4 group-32, INT8 group-64) on the
 // 5th-generation tensor cores (tcgen05, tensor memory, TMA).
 //
 // Computes the same thing as the mma.sync path in verify_attn.cu (see there
@@ -18,9 +19,12 @@
 //     warpgroup 0 combines both halves.
 //   * Warp 8 (producer): TMA-loads each page's K and V tiles (8 KB each,
 //     128-byte swizzle) into a ring of shared-memory stages, and stages the
-//     page's scale terms.
-//   * Warps 12-15 (converters): widen each page's V codes to fp16 (exact)
-//     into a second ring, laid out as the MN-major operand of the PV MMA.
+//     page's scale terms (FP8 formats; the row scales by bulk copies); the
+//     INT4 and INT8 codes and scales arrive by 1-D bulk copies.
+//   * Warps 12-15 (converters): widen each page's V codes to fp16 (exact for
+//     E4M3; FP8 row: times s_j / s_max; INT4 and INT8: times the group scale)
+//     into a second ring, laid out as the MN-major operand of the PV MMA; for
+//     INT4 and INT8 also the K codes, into a third ring.
 //   * Warps 9-11 issue tcgen05.mma, one thread each:
 //       warp 9 + j: S_j  = Q_hi K^T + Q_lo K^T  (kind::f8f6f4; A = Q from shared
 //                                                memory, B = the page's K tile)
@@ -29,12 +33,15 @@
 //     A thread waits on the order of a hundred cycles per tcgen05.mma it
 //     issues, whatever the tile's N, so a page's twelve instructions are
 //     spread over three issuing warps; the tensor core interleaves their
-//     streams.  Q is carried as the sum of two E4M3 terms (hi + lo, 8
-//     significant bits, like bf16); the K codes feed the tensor core as they
-//     are stored.
+//     streams.  FP8 formats: Q is carried as the sum of two E4M3 terms (hi +
+//     lo, 8 significant bits, like bf16) and the K codes feed the tensor core
+//     as they are stored.  INT4 and INT8: the QK is kind::f16 with fp16 Q
+//     and the converters' fp16 K.
 //   * Warps 0-3 / 4-7 (softmax warpgroup 0 / 1): thread t owns TMEM lane t =
 //     query row t.  Per page it reads its 64 scores, applies the page's K
-//     scale and the row's Q scale, masks the window's future keys, runs the
+//     scale (FP8 row: each key's) and the row's Q scale, masks the window's
+//     future keys (or, for a draft tree, the keys outside the row's ancestor
+//     set), runs the
 //     online softmax in the log2 domain (the page's V scale folded into the
 //     shift), rescales its O in tensor memory only when the running max
 //     outgrows a lag of kTau, and writes P as fp16 back to tensor memory.
@@ -111,8 +118,8 @@ struct Ctl {
   uint64_t empty[kStages];  // the stage's K was used by QK, its V converted, its scales read
   uint64_t v16_full[kV16Stages];   // fp16 V written (one arrival per converter warp)
   uint64_t v16_empty[kV16Stages];  // the PV that read it completed
-  uint64_t k16_full[kV16Stages];   // INT4: fp16 K written (one arrival per converter warp)
-  uint64_t k16_empty[kV16Stages];  // INT4: the QK that read it completed
+  uint64_t k16_full[kV16Stages];   // INT4 / INT8: fp16 K written (one arrival per converter warp)
+  uint64_t k16_empty[kV16Stages];  // INT4 / INT8: the QK that read it completed
   uint64_t s_full[2][2];    // [warpgroup j][buffer x]: QK of the buffer's page is in it
   uint64_t p_full[2][2];    // the warpgroup wrote P over the buffer
   uint64_t pv_done[2][2];   // the PV that read that P has completed (the buffer is free)
@@ -484,11 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   const uint32_t row_threads = 32u * (uint32_t)min(4, (a.R + 31) / 32);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kNS; ++s) {
-      // FP8: the copies' expect_tx arrival, then the scale terms; INT4: the
-      // copies' arrival (the scales are inside the stage)
+      // FP8 formats: the copies' expect_tx arrival, then the scale terms;
+      // INT4 / INT8: the copies' arrival (the scales are inside the stage)
       mbar_init(smem_u32(&ctl->full[s]), kDeq ? 1 : 2);
-      // FP8: QK commit (K tile), converters (V tile), softmax warps (scales);
-      // INT4: converters (K and V codes), softmax warps
+      // FP8 formats: QK commit (K tile), converters (V tile), softmax warps
+      // (scales); INT4 / INT8: converters (K and V codes), softmax warps
       mbar_init(smem_u32(&ctl->empty[s]), (kDeq ? 0 : 1) + 4 + row_threads / 32);
     }
     for (int t = 0; t < kV16Stages; ++t) {
@@ -689,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
         const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
-        // FP8: the page's K tile as loaded; INT4: its fp16 K from the converters
+        // FP8 formats: the page's K tile as loaded; INT4 / INT8: its fp16 K from the converters
         if (!(ok = kDeq ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit)
                          : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kNS) & 1), abort_flag, a.wait_limit)))
           break;

@@ -1,5 +1,5 @@
 // verify_attn_tc.cuh -- internal interface between the verify_attn entry
-// point and the tcgen05 (FP8) kernels of verify_attn_tc.cu.
+// points and the tcgen05 kernels of verify_attn_tc.cu.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -15,13 +15,14 @@ constexpr int kMaxLanesTc = 1024;  // lanes per call handled by the tcgen05 path
 
 struct TcArgs {
   const uint16_t* q;        // bf16 [B][W][Hq][128]
-  const uint8_t* k_codes;   // INT4 pools (the FP8 pools are read through tensor maps)
+  const uint8_t* k_codes;   // INT4 / INT8 pools (the FP8 pools are read through tensor maps)
   const uint8_t* v_codes;
   const int32_t* page_table;
   const int32_t* seq_lens;
   const int32_t* parent;  // draft tree [B][W] (slot 0 unused) or null for the causal window
   const int32_t* n_lane;  // window rows per lane (1 + d_b) or null for all `window` rows
-  const void* k_scales;  // FP8: f32 [pages][Hkv]; INT4: f16 [pages][Hkv][64][4]
+  const void* k_scales;  // FP8: f32 [pages][Hkv]; INT4: f16 [pages][Hkv][64][4];
+                         // INT8: f16 [pages][Hkv][64][2]; FP8 row: f32 [pages][Hkv][64]
   const void* v_scales;
   float2* ws_ml;  // [lanes * Hkv + ctas][R]
   float* ws_o;    // [lanes * Hkv + ctas][R][128]
