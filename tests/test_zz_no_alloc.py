@@ -43,7 +43,7 @@ def _reference(sdva, gcache, step, q, table, seq, max_context):
     return ref
 
 
-@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4])
+@pytest.mark.parametrize("dtype", [synth.KV_FP8, synth.KV_INT4, synth.KV_INT8, synth.KV_FP8_ROW])
 def test_noalloc_matches_workspace_call_large_then_small(dtype):
     """Two calls in a row through the C ABI: first a large case (8 lanes up to
     60,000 tokens, the scratch filled with its split-K partials), then a
@@ -55,7 +55,7 @@ def test_noalloc_matches_workspace_call_large_then_small(dtype):
 
     cases = [([3000, 700, 12000, 60000, 64, 9000, 31000, 150], 16, 31), ([500, 64, 1300], 8, 32)]
     for lens, W, seed in cases:
-        spec, step, gcache = _case(dtype, lens, W if dtype == synth.KV_FP8 else min(W, 8), seed)
+        spec, step, gcache = _case(dtype, lens, W if dtype in (synth.KV_FP8, synth.KV_FP8_ROW) else min(W, 8), seed)
         B, Wn, Hq = step.q.shape[:3]
         max_context = max(lens)
         q, table, seq = bf16_dev(step.q), i32_dev(step.page_table), i32_dev(step.seq_lens)
