@@ -530,6 +530,7 @@ int verify_launch(const sdva_kv_cache* cache, const void* q, int num_q_heads, in
     t.max_context = max_context;
     t.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     t.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+    t.unit_cost = tc::unit_cost_of(cache->dtype);
     return tc::launch_verify_tc(cache, t, num_sms, s, after_append);
   }
   // the mma.sync kernels (more than 128 rows per kv head) know only the

@@ -154,23 +154,23 @@ static_assert(Smem<SDVA_KV_FP8_ROW>::kOffStages % 1024 == 0 && Smem<SDVA_KV_FP8_
               "TMA tiles with the 128-byte swizzle start on 1024-byte boundaries");
 
 // Partition of the flattened (lane, kv head, page) list over the CTAs.  Each
-// unit (lane, kv head) costs its pages plus kUnitCost: a CTA that starts a
-// new unit inside its range pays a segment end and a segment start (an
-// output epilogue, a Q row load and a pipeline refill, measured at about the
-// time of 12-16 pages), so equal shares of cost, not of pages, end together.  CTA c
-// owns the cost interval [c T / Ce, (c + 1) T / Ce), T the total cost and Ce
-// = min(CTAs, T), mapped to real pages: the cost of a unit's start maps to
-// its first page.
-constexpr int kUnitCost = 16;
+// unit (lane, kv head) costs its pages plus a unit cost uc: a CTA that starts
+// a new unit inside its range pays a segment end and a segment start (an
+// output epilogue, a Q row load and a pipeline refill), so equal shares of
+// cost, not of pages, end together.  uc is that price in pages of the format
+// (measured: 20 for FP8 page scales, 16 for the formats whose pages take
+// longer: FP8 row scales, INT4, INT8).  CTA c owns the cost interval [c T / Ce, (c + 1) T / Ce), T the
+// total cost and Ce = min(CTAs, T), mapped to real pages: the cost of a
+// unit's start maps to its first page.
 struct Partition {
   const int* pref;  // [B + 1] pages per kv head of lanes < b
-  const int* cp;    // [B + 1] cost per kv head of lanes < b (pages + kUnitCost per lane with pages)
-  int B, Hkv;
+  const int* cp;    // [B + 1] cost per kv head of lanes < b (pages + uc per lane with pages)
+  int B, Hkv, uc;
   __device__ long long total_pages() const { return (long long)Hkv * pref[B]; }
   __device__ long long total_cost() const { return (long long)Hkv * cp[B]; }
   __device__ long long ctas(int C) const { return min((long long)C, total_cost()); }
   // real flattened page position of cost position y (0 <= y <= total cost).
-  // The offset inside a lane, below Hkv * (pages + kUnitCost), fits in 32
+  // The offset inside a lane, below Hkv * (pages + uc), fits in 32
   // bits: this path requires num_pages * Hkv * 64 < 2^31.
   __device__ long long real_of(long long y) const {
     if (y >= total_cost()) return total_pages();
@@ -184,9 +184,9 @@ struct Partition {
     }
     const int nb = pref[lo + 1] - pref[lo];
     const uint32_t r = (uint32_t)(y - (long long)Hkv * cp[lo]);
-    const uint32_t span = (uint32_t)(nb + kUnitCost);
+    const uint32_t span = (uint32_t)(nb + uc);
     const uint32_t q = r / span, v = r - q * span;
-    return (long long)Hkv * pref[lo] + (long long)q * nb + max(0, (int)v - kUnitCost);
+    return (long long)Hkv * pref[lo] + (long long)q * nb + max(0, (int)v - uc);
   }
   // floor(c T / Ce), 0 <= c <= Ce <= 1024, in 32-bit arithmetic (T < 2^31):
   // c T / Ce = c (T / Ce) + c (T % Ce) / Ce
@@ -211,9 +211,10 @@ struct Partition {
 };
 
 // Warp-wide prefix over lanes (one warp, all lanes): pref[b] = pages per kv
-// head of lanes < b and cp[b] = their cost (pages + kUnitCost per lane with
+// head of lanes < b and cp[b] = their cost (pages + unit_cost per lane with
 // pages), b = 0 .. B; lens[b] = L_b when lens is not null.
 __device__ __forceinline__ void partition_prefix(const int32_t* seq_lens, int B, int W, int max_context, int max_pages,
+                                                 int unit_cost,
                                                  int lane, int* pref, int* cp, int* lens) {
   int carry = 0, carry_c = 0;
   for (int b0 = 0; b0 < B; b0 += 32) {
@@ -225,7 +226,7 @@ __device__ __forceinline__ void partition_prefix(const int32_t* seq_lens, int B,
       const bool ok = L >= 0 && L <= max_context && (long long)L + W <= (long long)max_pages * kPage;
       n = ok ? (L + W + kPage - 1) / kPage : 0;
     }
-    const int cost = n > 0 ? n + kUnitCost : 0;
+    const int cost = n > 0 ? n + unit_cost : 0;
     int incl = n, incl_c = cost;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -478,11 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
 
   // ---- partition: pages and cost per kv head of every lane, prefix over lanes ----
   if (warp == 0) {
-    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, lane, ctl->pref, ctl->cp, ctl->lens);
+    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, a.unit_cost, lane, ctl->pref, ctl->cp,
+                     ctl->lens);
     __syncwarp();
     if (lane < 2) {
       // this CTA's page range [start, end): start on lane 0, end on lane 1
-      const Partition part{ctl->pref, ctl->cp, a.B, a.Hkv};
+      const Partition part{ctl->pref, ctl->cp, a.B, a.Hkv, a.unit_cost};
       const long long Ce = part.ctas(C);
       ctl->range[lane] = c < Ce ? part.cta_begin(c + lane, Ce) : 0;
     }
@@ -1257,13 +1259,13 @@ __device__ __forceinline__ bool merge_locate(const TcArgs& a, int C, int b, int 
   const int L = a.seq_lens[b];
   const bool len_ok = L >= 0 && L <= a.max_context && (long long)L + a.W <= (long long)a.max_pages * kPage;
   if (warp == 0) {
-    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, lane, pref, cp, nullptr);
+    partition_prefix(a.seq_lens, a.B, a.W, a.max_context, a.max_pages, a.unit_cost, lane, pref, cp, nullptr);
     __syncwarp();
     if (lane == 0 && len_ok) {
-      const Partition part{pref, cp, a.B, a.Hkv};
+      const Partition part{pref, cp, a.B, a.Hkv, a.unit_cost};
       const int nb = pref[b + 1] - pref[b];
       // cost position of the unit's first page (after its start cost)
-      const long long y0 = (long long)a.Hkv * cp[b] + (long long)hk * (nb + kUnitCost) + kUnitCost;
+      const long long y0 = (long long)a.Hkv * cp[b] + (long long)hk * (nb + a.unit_cost) + a.unit_cost;
       const long long Ce = part.ctas(C);
       *s_first = part.cta_of_cost(y0, Ce);
       *s_last = part.cta_of_cost(y0 + nb - 1, Ce);
@@ -1509,6 +1511,10 @@ cudaError_t launch_split(void (*kern)(CUtensorMap, CUtensorMap, TcArgs), const C
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
 }
 
+int unit_cost_of(int dtype) {
+  return dtype == SDVA_KV_FP8_E4M3 ? 20 : 16;
+}
+
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms) {
   const int R = W * (Hq / Hkv);
   const size_t slots = (size_t)B * Hkv + (size_t)num_sms;
@@ -1523,7 +1529,7 @@ bool tc_supported(const sdva_kv_cache* cache, int B, int W, int Hq, int max_page
   const bool dtype_ok = cache->dtype == SDVA_KV_INT4_G32 || cache->dtype == SDVA_KV_INT8_G64 ||
                         ((cache->dtype == SDVA_KV_FP8_E4M3 || cache->dtype == SDVA_KV_FP8_ROW) && encoder() != nullptr);
   // the partition's cost arithmetic is 32-bit (see Partition)
-  const bool cost_ok = (long long)B * (max_pages + kUnitCost) * Hkv < (1LL << 31);
+  const bool cost_ok = (long long)B * (max_pages + unit_cost_of(cache->dtype)) * Hkv < (1LL << 31);
   return dtype_ok && cost_ok && R <= 128 && B <= kMaxLanesTc && num_sms > 0 && num_sms <= kMaxSegments &&
          (long long)cache->num_pages * Hkv * kPage < (1LL << 31);
 }

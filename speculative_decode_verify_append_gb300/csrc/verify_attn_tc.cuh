@@ -30,9 +30,12 @@ struct TcArgs {
   int32_t* status;
   int num_pages, B, Hkv, Hq, G, W, R, max_pages, max_context;
   long long wait_limit;  // clock cycles a device wait may take before the CTA gives up
+  int unit_cost;         // price of a unit's start in the partition, in pages (unit_cost_of)
   float sm_scale_log2;
 };
 
+// The partition's price of starting a unit, in pages of the cache format.
+int unit_cost_of(int dtype);
 // Scratch bytes of the tcgen05 path (split-K partials, one slot per unit and per CTA).
 size_t tc_workspace_bytes(int B, int W, int Hq, int Hkv, int num_sms);
 // Whether the tcgen05 path handles this call (<= 128 rows per kv head, ...).

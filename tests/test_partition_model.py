@@ -1,8 +1,10 @@
 """Host-side model of the verify kernel's cost-balanced partition (no GPU).
 
 The split kernel's CTAs cut equal shares of a cost that counts every
-(lane, kv head) unit as its pages plus 16 page-equivalents (the price of
-starting a unit), map their cost interval back to page positions, and the
+(lane, kv head) unit as its pages plus a unit cost (the price of starting a
+unit, in pages of the cache format: 20 for FP8 page scales, 16 for the
+others), map
+their cost interval back to page positions, and the
 merge finds a unit's first and last CTA from cost positions.  This model
 states those rules in Python and checks the invariants the kernel relies on
 at sizes the GPU tests do not reach: the CTAs' page ranges tile every page
@@ -12,10 +14,10 @@ agree with exact arithmetic for every total cost below 2^31."""
 import numpy as np
 import pytest
 
-UNIT_COST = 16
+UNIT_COSTS = (16, 20)  # FP8 row, INT4, INT8; FP8 page scales
 
 
-def prefix(pages):
+def prefix(pages, UNIT_COST):
     pref, cp = [0], [0]
     for n in pages:
         pref.append(pref[-1] + n)
@@ -23,7 +25,7 @@ def prefix(pages):
     return pref, cp
 
 
-def real_of(y, pref, cp, H):
+def real_of(y, pref, cp, H, UNIT_COST):
     B = len(pref) - 1
     if y >= H * cp[B]:
         return H * pref[B]
@@ -55,13 +57,13 @@ def cta_of_cost(y, ce, T):
     return c
 
 
-def check(pages, H, C):
-    pref, cp = prefix(pages)
+def check(pages, H, C, UNIT_COST):
+    pref, cp = prefix(pages, UNIT_COST)
     T, P = H * cp[-1], H * pref[-1]
     if T == 0:
         return
     ce = min(C, T)
-    begins = [real_of(cost_begin_u32(c, ce, T), pref, cp, H) for c in range(ce + 1)]
+    begins = [real_of(cost_begin_u32(c, ce, T), pref, cp, H, UNIT_COST) for c in range(ce + 1)]
     assert begins[0] == 0 and begins[-1] == P
     assert all(begins[i] <= begins[i + 1] for i in range(ce))
     for b, nb in enumerate(pages):
@@ -76,18 +78,20 @@ def check(pages, H, C):
                 assert holds == (f <= c <= l), (pages, H, C, b, hk, c, f, l)
 
 
-def test_random_lane_mixes_tile_and_invert():
+@pytest.mark.parametrize("unit_cost", UNIT_COSTS)
+def test_random_lane_mixes_tile_and_invert(unit_cost):
     rng = np.random.default_rng(5)
     for _ in range(600):
         B = int(rng.integers(1, 40))
         pages = [int(rng.choice([0, 1, 2, rng.integers(1, 50), rng.integers(1, 2000)])) for _ in range(B)]
-        check(pages, int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 3, 148, 152, 1024])))
+        check(pages, int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 3, 148, 152, 1024])), unit_cost)
 
 
-def test_workload_shapes():
-    check([114, 290, 394, 487, 491, 864, 978, 1011], 4, 148)  # eight lanes of 4k..64k tokens
-    check([3751], 4, 148)                                       # one lane of 240,000 tokens
-    check([512], 4, 148)                                        # plain decode of 32,768 tokens
+@pytest.mark.parametrize("unit_cost", UNIT_COSTS)
+def test_workload_shapes(unit_cost):
+    check([114, 290, 394, 487, 491, 864, 978, 1011], 4, 148, unit_cost)  # eight lanes of 4k..64k tokens
+    check([3751], 4, 148, unit_cost)                                       # one lane of 240,000 tokens
+    check([512], 4, 148, unit_cost)                                        # plain decode of 32,768 tokens
 
 
 @pytest.mark.parametrize("T", [1, 7, 1023, 1024, 2**20 + 3, 2**31 - 1, 2**31 - 1025, 1_500_000_017])
