@@ -60,9 +60,9 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order, comments stripped);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "f7074bccaab392bef674ed63b44a2a5b668334679699e331f3b4aa10ffd5c8b3",
-               "bytes": {"multi_lane": 314599680, "long_context": 249038848, "int4_12slot": 338024448,
-                         "multi_lane_int8": 323879168, "multi_lane_fp8row": 324170240}}
+NCU_TRAFFIC = {"sources_sha256": "db40469917dead2019db5fac0a2230a070675be9b02e66e0869e9b39cdda9b25",
+               "bytes": {"multi_lane": 314612480, "long_context": 249106176, "int4_12slot": 337938176,
+                         "multi_lane_int8": 323832832, "multi_lane_fp8row": 323821568}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
