@@ -253,3 +253,56 @@ def test_verify_step_in_a_cuda_graph():
     assert torch.equal(vs.out, eager[0]) and torch.equal(vs.accept_len, eager[1])
     assert torch.equal(vs.out_tokens, eager[2])
     assert int(vs.status.item()) == 0
+
+
+@pytest.mark.parametrize("V,W,Hq,Hkv,offset", [
+    (151936, 16, 24, 4, 0),   # 96 rows per kv head, vector loads of the logits
+    (32003, 8, 8, 1, 0),      # odd vocab: scalar loads
+    (4096, 8, 16, 2, 1),      # rows not 16-byte aligned: scalar loads
+    (4, 4, 8, 8, 0),          # one float4 per row
+    (151937, 16, 32, 4, 0),   # 128 rows per kv head
+], ids=["vec", "odd", "unaligned", "v4", "r128"])
+def test_verify_step_argmax_on_hostile_logits(V, W, Hq, Hkv, offset):
+    """verify_step's acceptance on logits with heavy ties, NaN rows and
+    half-NaN rows, signed zeros and -inf rows, on lanes so short that most
+    CTAs of the split kernel have no pages: tokens, accept lengths and
+    committed lengths equal the oracle's exactly, and the attention rows
+    equal the three calls' bit for bit."""
+    sdva, VerifyStep = _sdva()
+    lens = np.array([5, 64, 130, 1], np.int32)
+    B = len(lens)
+    rng = np.random.default_rng(V + W)
+    spec = synth.Spec("hostile", 5, B, 0, 0, Hq, Hkv, W, synth.KV_FP8, V, 0.7, True)
+    table, total = synth.page_table_for(spec, lens + W, W)
+    stp = synth.make_step(spec, seq_lens=lens, with_accept=False)
+    stp.page_table, stp.num_pages = table, total
+    caches = [fill_both(spec, stp, with_oracle=False)[0] for _ in range(2)]
+    logits = rng.integers(-2, 3, size=(B, W, V)).astype(np.float32)
+    logits[0, 0, :] = np.nan
+    logits[1, 1, : V // 2] = np.nan
+    logits[2, 2, :] = -0.0
+    logits[2, 2, V - 1] = 0.0
+    logits[3, 3, :] = -np.inf
+    drafts = np.argmax(np.nan_to_num(logits, nan=-9.0), axis=2)[:, :W - 1].astype(np.int32)
+    drafts[1, 2] = (drafts[1, 2] + 1) % V  # one lane rejects in the middle
+    flat = torch.from_numpy(logits.reshape(-1))
+    buf = torch.empty(flat.numel() + offset, dtype=torch.float32, device="cuda")
+    lg = buf[offset:].view(logits.shape)
+    lg.copy_(flat.view(logits.shape))
+    dr = i32_dev(drafts)
+    tdev = i32_dev(table)
+    q, kw, vw = bf16_dev(stp.q), bf16_dev(stp.k_win), bf16_dev(stp.v_win)
+    va, vb = (VerifyStep(B, W, Hq, Hkv, int(lens.max()) + W, V) for _ in range(2))
+    La, Lb = i32_dev(lens), i32_dev(lens)
+    # both caches hold the window already (fill_both); both sides append it again
+    va.run(caches[0], q, kw, vw, tdev, La, lg, dr, commit=True)
+    vb.step(caches[1], q, kw, vw, tdev, Lb, lg, dr, commit=True)
+    torch.cuda.synchronize()
+    acc, tok, newL, st = oracle.spec_accept(logits, drafts, lens)
+    assert np.array_equal(vb.out_tokens.cpu().numpy(), tok)
+    assert np.array_equal(vb.accept_len.cpu().numpy(), acc)
+    assert np.array_equal(Lb.cpu().numpy(), newL)
+    assert int(vb.status.item()) == st == 0
+    assert torch.equal(va.out, vb.out)
+    assert torch.equal(va.out_tokens, vb.out_tokens) and torch.equal(va.accept_len, vb.accept_len)
+    assert torch.equal(La, Lb)
