@@ -810,6 +810,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     // exact.  Thread u handles the 16-byte source chunks u, u + 128, ...
     // ------------------------------------------------------------------
     const int u = threadIdx.x - kConvWarp * 32;
+    // Shared memory serves a warp's 16-byte accesses a quarter-warp (8
+    // lanes) at a time, and the two 8 KB halves of an fp16 tile share banks:
+    // each quarter-warp takes two rows whose stores land in 8 distinct
+    // 16-byte bank groups (as do its loads).  Lane l of a warp covering rows
+    // r0 .. : row offset rof, 16-dim chunk c8 (FP8, INT8) or group g4 (INT4).
+    const int q8 = lane >> 3, rr = (lane >> 2) & 1;
+    const int c8 = (lane & 3) + 4 * (rr ^ (q8 & 1));                        // rows r0 + rof, 4 per warp
+    const int rof8 = 2 * (q8 >> 1) + rr;
+    const int hb = (lane >> 2) & 1, r4 = (lane >> 1) & 1;                   // INT4: 8 rows per warp
+    const int g4 = (lane & 1) + 2 * (hb ^ (q8 & 1));
+    const int rof4 = 4 * (q8 >> 1) + 2 * hb + r4;
     bool ok = true;
     for (long long h = 0; h < n_local && ok; ++h) {
       const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
@@ -829,8 +840,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
 #pragma unroll 4
         for (int q = 0; q < 8; ++q) {
-          const int item = u + 128 * q;  // 1024 chunks per page
-          const int tk = item >> 9, r = (item >> 3) & 63, c = item & 7;
+          const int item = u + 128 * q;  // 1024 chunks per page, 32 per warp: 4 rows x 8 chunks
+          const int tk = item >> 9, r = 4 * ((item & 511) >> 5) + rof8, c = c8;
           const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 128 + c * 16);
           const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes +
                                                                  r * 4 + (c >> 2) * 2);
@@ -849,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int item = u + 128 * q;  // 512 groups per page
-          const int tk = item >> 8, r = (item >> 2) & 63, gi = item & 3;
+          const int item = u + 128 * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
+          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
           const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
           const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
           uint4 ch[4];
@@ -875,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-        const int item = u + 128 * q;
-        const int r = item >> 3, c = item & 7;  // key row, 16-dim chunk
+        const int item = u + 128 * q;  // 512 chunks per page, 32 per warp: 4 rows x 8 chunks
+        const int r = 4 * (item >> 5) + rof8, c = c8;  // key row, 16-dim chunk
         const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
         const uint32_t b[4] = {w.x, w.y, w.z, w.w};
         uint32_t h16[8];
