@@ -9,8 +9,10 @@
 // Kernel 1 (argmax): one thread-block cluster of up to 8 CTAs per logits
 // row; each CTA scans a contiguous slice of the row with 16-byte streaming
 // loads, four in flight per thread (32 registers, so eight 256-thread CTAs fit
-// on an SM and the grid of the multi-row case is a single wave), reduces
-// (value, index) in shared memory,
+// on an SM and the grid of the multi-row case is a single wave), keeps its
+// best with one greater-than test per element (exact, since a thread meets
+// its elements in index order; a thread that met nothing above -inf rescans
+// them in the full order), reduces (value, index) in shared memory,
 // and stores it into CTA rank 0's shared memory through distributed shared
 // memory; rank 0 writes the row's argmax.  No global scratch.  Ties go to the
 // lowest index, NaN never wins, an all-NaN row gives 0.
@@ -80,6 +82,67 @@ __device__ __forceinline__ void take4(const float4 v, int i, float& bv, int& bi)
   take(v.w, i + 3, bv, bi);
 }
 
+// One thread meets its elements in increasing index order.  Once its best
+// holds a number above -inf, "v > best" alone keeps the order of take (an
+// equal value comes later and loses, NaN compares false) at a third of the
+// instructions.  Scans start from (-inf, none) in that form; a thread that met
+// nothing above -inf (no element, or only -inf and NaN) scans its elements
+// again in the exact form.
+__device__ __forceinline__ void take_gt(float v, int i, float& bv, int& bi) {
+  if (v > bv) {
+    bv = v;
+    bi = i;
+  }
+}
+template <bool kExact>
+__device__ __forceinline__ void take4_as(const float4 v, int i, float& bv, int& bi) {
+  if constexpr (kExact) {
+    take4(v, i, bv, bi);
+  } else {
+    take_gt(v.x, i, bv, bi);
+    take_gt(v.y, i + 1, bv, bi);
+    take_gt(v.z, i + 2, bv, bi);
+    take_gt(v.w, i + 3, bv, bi);
+  }
+}
+constexpr int kNone = 0x7fffffff;
+__device__ __forceinline__ float nan_f() { return __int_as_float(0x7fffffff); }
+
+// float4 k, k + step, ... below kend of x4 (element index 4 k), kLoads
+// 16-byte streaming loads in flight
+template <bool kExact, int kLoads>
+__device__ __forceinline__ void scan_vec(const float4* x4, int k, int kend, int step, float& bv, int& bi) {
+  for (; k + (kLoads - 1) * step < kend; k += kLoads * step) {
+    float4 v[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) v[u] = __ldcs(x4 + k + u * step);
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) take4_as<kExact>(v[u], 4 * (k + u * step), bv, bi);
+  }
+  for (; k < kend; k += step) take4_as<kExact>(__ldcs(x4 + k), 4 * k, bv, bi);
+}
+// the argmax of one thread's elements x[k], x[k + step], ... below end, in
+// the order of take
+template <int kLoads>
+__device__ __forceinline__ void thread_argmax_vec(const float4* x4, int k, int kend, int step, float& bv, int& bi) {
+  bv = -INFINITY;
+  bi = kNone;
+  scan_vec<false, kLoads>(x4, k, kend, step, bv, bi);
+  if (bi == kNone) {
+    bv = nan_f();
+    scan_vec<true, kLoads>(x4, k, kend, step, bv, bi);
+  }
+}
+__device__ __forceinline__ void thread_argmax(const float* x, int k, int end, int step, float& bv, int& bi) {
+  bv = -INFINITY;
+  bi = kNone;
+  for (int j = k; j < end; j += step) take_gt(x[j], j, bv, bi);
+  if (bi == kNone) {
+    bv = nan_f();
+    for (int j = k; j < end; j += step) take(x[j], j, bv, bi);
+  }
+}
+
 // grid (parts, rows), cluster (parts, 1, 1).  kVec: vocab % 4 == 0 and logits
 // is 16-byte aligned, so every row starts on a 16-byte boundary.
 // num_drafts (lazy form, nullable): rows past a lane's count, and every row of
@@ -98,24 +161,13 @@ __global__ void __launch_bounds__(kArgmaxThreads, 8) argmax_rows_kernel(const fl
   }
   const float* x = logits + (size_t)row * vocab;
   const int lo = part * chunk, hi = min(vocab, lo + chunk);
-  float bv = __int_as_float(0x7fffffff);  // NaN: loses to every number
-  int bi = 0x7fffffff;
+  float bv;
+  int bi;
   if constexpr (kVec) {
     // chunk is a multiple of 4: every slice starts on a 16-byte boundary
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    const int step = blockDim.x;
-    int k = lo / 4 + threadIdx.x;
-    const int kend = hi / 4;
-    for (; k + 3 * step < kend; k += 4 * step) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + k + u * step);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) take4(v[u], 4 * (k + u * step), bv, bi);
-    }
-    for (; k < kend; k += step) take4(__ldcs(x4 + k), 4 * k, bv, bi);
+    thread_argmax_vec<4>(reinterpret_cast<const float4*>(x), lo / 4 + threadIdx.x, hi / 4, blockDim.x, bv, bi);
   } else {
-    for (int k = lo + threadIdx.x; k < hi; k += blockDim.x) take(x[k], k, bv, bi);
+    thread_argmax(x, lo + threadIdx.x, hi, blockDim.x, bv, bi);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -220,24 +272,15 @@ __global__ void __launch_bounds__(kWalkThreads, 4)
   int i = 0;
   for (;; ++i) {
     const float* x = rows + (size_t)i * vocab;
-    float bv = __int_as_float(0x7fffffff);  // NaN: loses to every number
-    int bi = 0x7fffffff;
+    float bv;
+    int bi;
     if constexpr (kVec) {
       // row i + 1 is needed only if draft i agrees: start its fetch into L2 now
       if (threadIdx.x == 0 && i < d && hi > lo) prefetch_l2_bulk(x + vocab + lo, (uint32_t)(hi - lo) * 4u);
-      const float4* x4 = reinterpret_cast<const float4*>(x);
-      const int kend = hi >> 2;
-      for (int k0 = (lo >> 2) + threadIdx.x; k0 < kend; k0 += kWalkLoads * kWalkThreads) {
-        float4 v[kWalkLoads];
-#pragma unroll
-        for (int u = 0; u < kWalkLoads; ++u)
-          if (k0 + u * kWalkThreads < kend) v[u] = __ldcs(x4 + k0 + u * kWalkThreads);
-#pragma unroll
-        for (int u = 0; u < kWalkLoads; ++u)
-          if (k0 + u * kWalkThreads < kend) take4(v[u], 4 * (k0 + u * kWalkThreads), bv, bi);
-      }
+      thread_argmax_vec<kWalkLoads>(reinterpret_cast<const float4*>(x), (lo >> 2) + threadIdx.x, hi >> 2, kWalkThreads,
+                                    bv, bi);
     } else {
-      for (int k = lo + threadIdx.x; k < hi; k += kWalkThreads) take(x[k], k, bv, bi);
+      thread_argmax(x, lo + threadIdx.x, hi, kWalkThreads, bv, bi);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {

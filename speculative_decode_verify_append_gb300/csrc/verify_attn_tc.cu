@@ -858,14 +858,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
         // it is the K-major operand of the QK MMA)
         uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
+        uint4 codes4[4];
+        uint32_t sc4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int item = u + 128 * q;
+          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
+          codes4[q] = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
+          sc4[q] = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int item = u + 128 * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
           const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
-          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
           uint4 ch[4];
-          int4_group_to_f16(codes, sc, ch);
+          int4_group_to_f16(codes4[q], sc4[q], ch);
           // dims 32gi .. 32gi + 31 -> region gi >> 1, 8-dim chunks 4 (gi & 1) .. + 3
           uint8_t* reg = (tk ? dst : kdst) + (gi >> 1) * 8192 + r * 128;
 #pragma unroll
