@@ -5,7 +5,7 @@
 // Computes the same thing as the mma.sync path in verify_attn.cu (see there
 // and sdva.h): every window row attends over keys 0 .. L_b + i of its kv head.
 //
-// Design (one persistent CTA of 16 warps per SM):
+// Design (one persistent CTA of 16 warps per SM; 20 for INT8):
 //   * Work = the flattened list of (lane, kv head, page) triples, cut into one
 //     contiguous range per CTA by cost (a unit's pages plus a fixed start cost,
 //     see Partition), computed on the device from seq_lens, so the launch
@@ -21,7 +21,7 @@
 //     128-byte swizzle) into a ring of shared-memory stages, and stages the
 //     page's scale terms (FP8 formats; the row scales by bulk copies); the
 //     INT4 and INT8 codes and scales arrive by 1-D bulk copies.
-//   * Warps 12-15 (converters): widen each page's V codes to fp16 (exact for
+//   * Warps 12-15, 12-19 for INT8 (converters): widen each page's V codes to fp16 (exact for
 //     E4M3; FP8 row: times s_j / s_max; INT4 and INT8: times the group scale)
 //     into a second ring, laid out as the MN-major operand of the PV MMA; for
 //     INT4 and INT8 also the K codes, into a third ring.
@@ -67,8 +67,8 @@ constexpr int kV16Bytes = 16384;     // fp16 K or V of one page: dims 0-63 | dim
 constexpr int kProducerWarp = 8;
 constexpr int kQkWarp = 9;           // + warpgroup index
 constexpr int kPvWarp = 11;
-constexpr int kConvWarp = 12;        // converters: warps 12-15
-constexpr int kThreads = 16 * 32;
+constexpr int kConvWarp = 12;        // converters: warps 12 .. 12 + Smem<KVT>::kConvWarps - 1
+constexpr int kThreads = 16 * 32;    // the block of the formats with four converter warps
 // Shared memory: the fp16 V ring, the fp16 K ring (INT4 and INT8), the K/V
 // code stages, the row-scale stages (FP8 row), then Ctl.  A stage holds one
 // (page, kv head): FP8 K and V tiles (TMA, 128-byte swizzle, 1024-byte
@@ -85,6 +85,12 @@ struct Smem {
   static constexpr uint32_t kScaleBytes = kInt4 ? 512 : 256;   // INT4 / INT8: 64 rows of fp16 group scales
   static constexpr uint32_t kStageBytes = kDeq ? 2 * kCodeBytes + 2 * kScaleBytes : 2 * kTileBytes;
   static constexpr int kNumStages = kInt8 ? 5 : kStages;
+  // converter warps 12 .. 12 + kConvWarps - 1: eight (two per sub-partition)
+  // for INT8, whose widening of K and V is on the page's critical path (eight
+  // measured 120.3 against 125.5 us multi-lane; INT4 gained nothing)
+  static constexpr int kConvWarps = kInt8 ? 8 : 4;
+  // the split of the 64K registers (setmaxnreg) for this block size
+  static constexpr int kThreads = (12 + kConvWarps) * 32;
   static constexpr uint32_t kOffV16 = 0;
   static constexpr uint32_t kOffK16 = kOffV16 + kV16Stages * kV16Bytes;
   static constexpr uint32_t kOffQ = kOffK16 + (kDeq ? kV16Stages * kV16Bytes : 0);
@@ -97,6 +103,10 @@ struct Smem {
 constexpr int kRegsSoftmax = 176;
 constexpr int kRegsOther = 80;
 static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther <= kThreads * 128, "register split");
+// INT8 (20 warps, launched at 96 registers: 61,440 for the block): softmax
+// 160, producer and issuers 56, the eight converter warps 48
+constexpr int kRegsSoftmax20 = 160, kRegsIss20 = 56, kRegsConv20 = 48;
+static_assert(256 * kRegsSoftmax20 + 128 * kRegsIss20 + 256 * kRegsConv20 <= 640 * 96, "register split (20 warps)");
 // tensor memory columns
 // S buffer x of warpgroup j: 64 fp32 columns of scores; once they are in
 // registers the warpgroup writes its P (64 keys of fp16 = 32 columns) over
@@ -459,7 +469,7 @@ __device__ __forceinline__ float row_vscale_max(const float* rs, int nv, int lan
 // per lane (a.n_lane).  Mode 0, the causal window, is the common case.
 constexpr int kModeTree = 1, kModeRagged = 2;
 template <int KVT, int kMode>
-__global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                     const __grid_constant__ CUtensorMap map_v,
                                                                     TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -498,12 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
       mbar_init(smem_u32(&ctl->full[s]), kDeq ? 1 : 2);
       // FP8 formats: QK commit (K tile), converters (V tile), softmax warps
       // (scales); INT4 / INT8: converters (K and V codes), softmax warps
-      mbar_init(smem_u32(&ctl->empty[s]), (kDeq ? 0 : 1) + 4 + row_threads / 32);
+      mbar_init(smem_u32(&ctl->empty[s]), (kDeq ? 0 : 1) + SM::kConvWarps + row_threads / 32);
     }
     for (int t = 0; t < kV16Stages; ++t) {
-      mbar_init(smem_u32(&ctl->v16_full[t]), 4);
+      mbar_init(smem_u32(&ctl->v16_full[t]), SM::kConvWarps);
       mbar_init(smem_u32(&ctl->v16_empty[t]), 1);
-      mbar_init(smem_u32(&ctl->k16_full[t]), 4);
+      mbar_init(smem_u32(&ctl->k16_full[t]), SM::kConvWarps);
       mbar_init(smem_u32(&ctl->k16_empty[t]), 1);
     }
     for (int j = 0; j < 2; ++j)
@@ -536,7 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
   // Each warpgroup changes its register budget as a whole, before its warps
   // take their roles.
   if (warp >= 8) {
-  regs_decrease<kRegsOther>();
+  if constexpr (SM::kConvWarps == 8) {
+    if (warp >= kConvWarp) regs_decrease<kRegsConv20>(); else regs_decrease<kRegsIss20>();
+  } else {
+    regs_decrease<kRegsOther>();
+  }
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------
     // producer: page ids and scales prefetched 32 pages at a time, two
@@ -810,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     // exact.  Thread u handles the 16-byte source chunks u, u + 128, ...
     // ------------------------------------------------------------------
     const int u = threadIdx.x - kConvWarp * 32;
+    constexpr int kCT = 32 * SM::kConvWarps;  // converter threads
     // Shared memory serves a warp's 16-byte accesses a quarter-warp (8
     // lanes) at a time, and the two 8 KB halves of an fp16 tile share banks:
     // each quarter-warp takes two rows whose stores land in 8 distinct
@@ -839,8 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         // operand of the QK MMA; V: the MN-major operand of the PV MMA)
         uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
 #pragma unroll 4
-        for (int q = 0; q < 8; ++q) {
-          const int item = u + 128 * q;  // 1024 chunks per page, 32 per warp: 4 rows x 8 chunks
+        for (int q = 0; q < 1024 / kCT; ++q) {
+          const int item = u + kCT * q;  // 1024 chunks per page, 32 per warp: 4 rows x 8 chunks
           const int tk = item >> 9, r = 4 * ((item & 511) >> 5) + rof8, c = c8;
           const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 128 + c * 16);
           const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes +
@@ -858,18 +873,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
         // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
         // it is the K-major operand of the QK MMA)
         uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
-        uint4 codes4[4];
-        uint32_t sc4[4];
+        constexpr int kQ = 512 / kCT;
+        uint4 codes4[kQ];
+        uint32_t sc4[kQ];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int item = u + 128 * q;
+        for (int q = 0; q < kQ; ++q) {
+          const int item = u + kCT * q;
           const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
           codes4[q] = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
           sc4[q] = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int item = u + 128 * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
+        for (int q = 0; q < kQ; ++q) {
+          const int item = u + kCT * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
           const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
           uint4 ch[4];
           int4_group_to_f16(codes4[q], sc4[q], ch);
@@ -930,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_tc_kernel(const __gr
     if (!ok) fail(ctl, a.status);
   }
   } else {
-    regs_increase<kRegsSoftmax>();
+    regs_increase<SM::kConvWarps == 8 ? kRegsSoftmax20 : kRegsSoftmax>();
     // ------------------------------------------------------------------
     // softmax warpgroups: wg 0 = warps 0-3 (even positions), wg 1 = warps
     // 4-7 (odd positions); thread = query row = TMEM lane
@@ -1514,11 +1530,11 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows) {
 // The split kernel, one CTA per SM; with after_append, as a programmatic
 // dependent of the kernel before it on the stream (the append of verify_step).
 cudaError_t launch_split(void (*kern)(CUtensorMap, CUtensorMap, TcArgs), const CUtensorMap& mk,
-                         const CUtensorMap& mv, const TcArgs& args, int num_sms, size_t smem, cudaStream_t stream,
-                         bool after_append) {
+                         const CUtensorMap& mv, const TcArgs& args, int num_sms, size_t smem, int threads,
+                         cudaStream_t stream, bool after_append) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1573,7 +1589,8 @@ int launch_split_kvt(const sdva_kv_cache* cache, const TcArgs& args, int num_sms
   // on every call, for the device current now
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<KVT>()) != cudaSuccess)
     return SDVA_ERR_CUDA;
-  if (launch_split(kern, mk, mv, args, num_sms, smem_bytes<KVT>(), stream, after_append) != cudaSuccess)
+  if (launch_split(kern, mk, mv, args, num_sms, smem_bytes<KVT>(), Smem<KVT>::kThreads, stream, after_append) !=
+      cudaSuccess)
     return SDVA_ERR_CUDA;
   return SDVA_OK;
 }
