@@ -60,9 +60,9 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order, comments stripped);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "db40469917dead2019db5fac0a2230a070675be9b02e66e0869e9b39cdda9b25",
-               "bytes": {"multi_lane": 314612480, "long_context": 249106176, "int4_12slot": 337938176,
-                         "multi_lane_int8": 323832832, "multi_lane_fp8row": 323821568}}
+NCU_TRAFFIC = {"sources_sha256": "73d2cee76990422002108d22bf9ab4cc77b83f03070cef5c06c82cb65293f755",
+               "bytes": {"multi_lane": 314643968, "long_context": 249052928, "int4_12slot": 337949184,
+                         "multi_lane_int8": 324120832, "multi_lane_fp8row": 323734528}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
