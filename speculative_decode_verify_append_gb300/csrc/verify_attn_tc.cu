@@ -89,7 +89,7 @@ struct Smem {
   // for INT8, whose widening of K and V is on the page's critical path (eight
   // measured 120.3 against 125.5 us multi-lane; INT4 gained nothing)
   static constexpr int kConvWarps = kInt8 ? 8 : 4;
-  // the split of the 64K registers (setmaxnreg) for this block size
+  // threads per block: softmax, producer and issuers, converters
   static constexpr int kThreads = (12 + kConvWarps) * 32;
   static constexpr uint32_t kOffV16 = 0;
   static constexpr uint32_t kOffK16 = kOffV16 + kV16Stages * kV16Bytes;
@@ -821,7 +821,8 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
     // -> fp16 in V16 slot g % kV16Stages: dims 0-63 and 64-127 as two
     // 64-row x 128-byte regions, each with the 128-byte swizzle (16-byte
     // chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  E4M3 -> fp16 is
-    // exact.  Thread u handles the 16-byte source chunks u, u + 128, ...
+    // exact.  Converter thread u handles the items u, u + kCT, ... of a page
+    // (kCT converter threads; the row and chunk of an item follow below).
     // ------------------------------------------------------------------
     const int u = threadIdx.x - kConvWarp * 32;
     constexpr int kCT = 32 * SM::kConvWarps;  // converter threads
