@@ -479,6 +479,9 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
   using SM = Smem<KVT>;
   constexpr bool kDeq = SM::kDeq, kRow = SM::kRow;
   constexpr int kNS = SM::kNumStages;
+  // A CTA's page positions are below 2^31, so ring slots and phases are taken
+  // in 32-bit unsigned arithmetic: a 64-bit division by 5 (INT8 stages) or 3
+  // (fp16 rings) on every page cost the INT8 call 3%.
   constexpr bool kTree = (kMode & kModeTree) != 0, kRagged = (kMode & kModeRagged) != 0;
   constexpr bool kSpinWait = !kDeq;  // see mbar_wait (the converters need the issue slots)
   constexpr uint32_t kStageBytes = SM::kStageBytes;
@@ -606,9 +609,9 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
           const long long g = g0 + i;
           const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
           const int ph = ph_m & ~kBadPage;
-          const int s = (int)(g % kNS);
+          const int s = (int)((uint32_t)g % (uint32_t)kNS);
           if (g >= kNS &&
-              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kNS - 1) & 1), abort_flag, a.wait_limit)))
+              !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)(((uint32_t)g / (uint32_t)kNS - 1) & 1), abort_flag, a.wait_limit)))
             break;
           if (lane == 0) {
             const int page_bad = (ph_m & kBadPage) ? 1 : 0;
@@ -645,8 +648,8 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
           const long long g = g0 + i;
           const int ph_m = __shfl_sync(0xffffffffu, ph_a, i);
           const int ph = ph_m & ~kBadPage;
-          const int s = (int)(g % kNS);
-          if (g >= kNS && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)((g / kNS - 1) & 1), abort_flag, a.wait_limit)))
+          const int s = (int)((uint32_t)g % (uint32_t)kNS);
+          if (g >= kNS && !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->empty[s]), (uint32_t)(((uint32_t)g / (uint32_t)kNS - 1) & 1), abort_flag, a.wait_limit)))
             break;
           const uint32_t bar = smem_u32(&ctl->full[s]);
           if (lane == 0) {
@@ -690,7 +693,7 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       // drain this CTA's own copies still in flight (bounded)
       for (long long g = max(0LL, issued - kNS); g < issued; ++g) {
         int dummy = 0;
-        mbar_wait<kSpinWait>(smem_u32(&ctl->full[g % kNS]), (uint32_t)((g / kNS) & 1), &dummy, 400000000LL);
+        mbar_wait<kSpinWait>(smem_u32(&ctl->full[(uint32_t)g % (uint32_t)kNS]), (uint32_t)(((uint32_t)g / (uint32_t)kNS) & 1), &dummy, 400000000LL);
       }
     }
   } else if (warp == kQkWarp || warp == kQkWarp + 1) {
@@ -711,10 +714,10 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->q_full), q_phase, abort_flag, a.wait_limit))) break;
       q_phase ^= 1u;
       for (long long h = first_own(g, j); h < g + seg_len; h += 2) {
-        const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
+        const int s = (int)((uint32_t)h % (uint32_t)kNS), t = (int)((uint32_t)h % (uint32_t)kV16Stages);
         // FP8 formats: the page's K tile as loaded; INT4 / INT8: its fp16 K from the converters
-        if (!(ok = kDeq ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit)
-                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kNS) & 1), abort_flag, a.wait_limit)))
+        if (!(ok = kDeq ? mbar_wait<kSpinWait>(smem_u32(&ctl->k16_full[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages) & 1), abort_flag, a.wait_limit)
+                         : mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)(((uint32_t)h / (uint32_t)kNS) & 1), abort_flag, a.wait_limit)))
           break;
         const long long n = h >> 1;  // the warpgroup's own page index
         const int x = (int)(n & 1);
@@ -781,12 +784,12 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       const long long seg_len = min((long long)(it.nb - it.p), n_local - g);
       bool fresh0 = true, fresh1 = true;
       for (long long h = g; h < g + seg_len; ++h) {
-        const int j = (int)(h & 1), t = (int)(h % kV16Stages);
+        const int j = (int)(h & 1), t = (int)((uint32_t)h % (uint32_t)kV16Stages);
         const long long n = h >> 1;  // the page's index among its warpgroup's pages
         const int x = (int)(n & 1);
         const bool fresh = j ? fresh1 : fresh0;
         if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->p_full[j][x]), (uint32_t)((n >> 1) & 1), abort_flag, a.wait_limit))) break;
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_full[t]), (uint32_t)((h / kV16Stages) & 1), abort_flag, a.wait_limit))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_full[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages) & 1), abort_flag, a.wait_limit))) break;
         fence_after_sync();
         if (lane == 0) {
           const uint32_t vt = v16 + t * kV16Bytes;
@@ -811,7 +814,7 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       fail(ctl, a.status);
       if (last >= 0) {
         int dummy = 0;
-        mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[last % kV16Stages]), (uint32_t)((last / kV16Stages) & 1), &dummy,
+        mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[(uint32_t)last % (uint32_t)kV16Stages]), (uint32_t)(((uint32_t)last / (uint32_t)kV16Stages) & 1), &dummy,
                   400000000LL);
       }
     }
@@ -839,13 +842,13 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
     const int rof4 = 4 * (q8 >> 1) + 2 * hb + r4;
     bool ok = true;
     for (long long h = 0; h < n_local && ok; ++h) {
-      const int s = (int)(h % kNS), t = (int)(h % kV16Stages);
-      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((h / kNS) & 1), abort_flag, a.wait_limit))) break;
+      const int s = (int)((uint32_t)h % (uint32_t)kNS), t = (int)((uint32_t)h % (uint32_t)kV16Stages);
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)(((uint32_t)h / (uint32_t)kNS) & 1), abort_flag, a.wait_limit))) break;
       if (h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
       if (kDeq && h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)((h / kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
         break;
       const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
       uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
@@ -1036,12 +1039,12 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
         if (!warp_active) continue;
         const int j = wg;
         const int p = p0 + (int)k;
-        const int s = (int)(g % kNS);
+        const int s = (int)((uint32_t)g % (uint32_t)kNS);
         const long long n = g >> 1;  // this warpgroup's own page index
         const int xb = (int)(n & 1);  // its S buffer
         if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->s_full[j][xb]), (uint32_t)((n >> 1) & 1), abort_flag, a.wait_limit))) break;
         // the producer staged the page's scale terms before completing full[s]
-        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)((g / kNS) & 1), abort_flag, a.wait_limit))) break;
+        if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)(((uint32_t)g / (uint32_t)kNS) & 1), abort_flag, a.wait_limit))) break;
         fence_after_sync();
         const float kscale = ctl->sk[s] * row_scale;
         float shift = ctl->shift[s], inv_f = ctl->inv_v[s];
