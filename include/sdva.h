@@ -430,8 +430,10 @@ int spec_accept_tree(const float* logits, int num_lanes, int window, int vocab, 
  *                drawn token at position a, -1 after.
  *   seq_lens_inout: nullable int32 [num_lanes] (in/out): adds 1 + a.
  *   workspace  : device memory of spec_accept_sampled_workspace_size()
- *                bytes, 8-byte aligned (per-row softmax statistics and
- *                per-slice sums of the drawn rows).
+ *                bytes, 8-byte aligned (per-row softmax statistics,
+ *                per-slice sums of the drawn rows and per-lane counters;
+ *                no initialisation needed, not shared by calls in flight
+ *                at the same time).
  * Arithmetic is fp32 (hardware exp2): a decision within fp32 rounding of its
  * boundary may differ from an exact evaluation.  An out-of-vocabulary draft
  * is a rejection and sets SDVA_STATUS_BAD_DRAFT.  window 1 .. 16,

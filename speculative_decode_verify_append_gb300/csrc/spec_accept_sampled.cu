@@ -12,20 +12,23 @@
 //
 // Kernel 1 (row statistics): one cluster of up to 8 CTAs per logits row; each
 // CTA reduces its slice to (running max, sum of exp) with 16-byte streaming
-// loads, the cluster combines the slices in rank order through distributed
-// shared memory, and rank 0 stores (M, S) of the row in the workspace.  All
-// rows are reduced at once over the whole GPU (the acceptance needs S of
-// every row up to the first rejection).
-// Kernels 2 and 3 (the draw, each a programmatic dependent of the one before):
-// up to 64 CTAs per lane.  Every CTA evaluates the ratio tests of the lane's
-// drafts identically, so all agree on a.  Kernel 2: each CTA walks its slice
-// of row a in tiles of 4 x 256 consecutive logits, a block scan giving the
-// running sum of the weights in index order, and stores the slice's total.
-// Kernel 3: every CTA adds the lane's totals in slice order; the CTA whose
-// running range holds the target walks its slice again with the same
-// arithmetic and stops inside the tile and the 4-logit group where the
-// running sum crosses it.  (One cluster of 8 CTAs per lane, the first
-// design, spent most of its time pulling a whole row through 8 SMs.)
+// loads, four in flight per thread, the cluster combines the slices in rank
+// order through distributed shared memory, and rank 0 stores (M, S) of the
+// row in the workspace.  All rows are reduced at once over the whole GPU (the
+// acceptance needs S of every row up to the first rejection).
+// Kernel 2 (the draw, a programmatic dependent of kernel 1): up to 64 CTAs per
+// lane.  Every CTA evaluates the ratio tests of the lane's drafts identically,
+// so all agree on a.  Each CTA walks its slice of row a in tiles of 4 x 256
+// consecutive logits (the loads of four tiles issued before the first is
+// scanned), a block scan giving the running sum of the weights in index
+// order, stores the slice's totals and counts itself in a per-lane counter
+// (zeroed by kernel 1).  The lane's last CTA adds the totals in slice order,
+// finds the slice whose running range holds the target, walks that slice
+// again with the same arithmetic and stops inside the tile and the 4-logit
+// group where the running sum crosses it.  No CTA waits for another.  (One
+// cluster of 8 CTAs per lane, the first design, spent most of its time
+// pulling a whole row through 8 SMs; a separate kernel for the walk to the
+// crossing cost one more dependent launch.)
 #include <cooperative_groups.h>
 
 #include "sdva_common.cuh"
@@ -74,9 +77,11 @@ __device__ __forceinline__ float4 load4(const float* x, int i, int end, float fi
 // grid (parts, rows), cluster (parts, 1, 1); stats[row] = (M, S)
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* logits, int vocab, int chunk,
-                                                            float2* stats) {
+                                                            float2* stats, int* counters, int num_lanes) {
   cg::cluster_group cluster = cg::this_cluster();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the draw kernel's per-lane arrival counters start at zero
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (int)blockIdx.y < num_lanes) counters[blockIdx.y] = 0;
   __shared__ Stat s_w[kThreads / 32];
   __shared__ Stat c_st[kMaxCluster];  // in rank 0: one entry per CTA of the cluster
   const int part = blockIdx.x, row = blockIdx.y;
@@ -84,10 +89,16 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* logits
   const int lo = part * chunk, hi = min(vocab, lo + chunk);
   Stat st = {0.0f, 0.0f};
   const float ninf = __int_as_float(0xff800000);
-  for (int i = lo + 4 * (int)threadIdx.x; i < hi; i += 4 * kThreads) {
-    const float4 v = load4<kVec>(x, i, hi, ninf);
-    st = add4(st, v);
+  // four 16-byte loads in flight per thread, folded in index order
+  int i = lo + 4 * (int)threadIdx.x;
+  for (; i + 12 * kThreads < hi; i += 16 * kThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = load4<kVec>(x, i + 4 * kThreads * u, hi, ninf);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) st = add4(st, v[u]);
   }
+  for (; i < hi; i += 4 * kThreads) st = add4(st, load4<kVec>(x, i, hi, ninf));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const Stat o = {__shfl_xor_sync(0xffffffffu, st.m, off), __shfl_xor_sync(0xffffffffu, st.s, off)};
@@ -149,54 +160,77 @@ __device__ __forceinline__ float weight(const Row& r, float lx, float qx) {
 }
 
 // Walk [lo, hi) in tiles of kTile logits, keeping the running sum of the
-// weights in index order.  search == false: returns the slice's total.
-// search == true: stops in the tile, the thread and the logit where the
-// running sum first exceeds `target` and stores that index in *found; when
-// it never does (the target sits within rounding of the slice's end), the
-// last index of positive weight.  Both modes do the same arithmetic, so a
-// target below the first mode's total is always crossed.
+// weights in index order; each thread's loads for kGroup tiles are issued
+// before the first of them is scanned.  search == false: returns the slice's
+// total (.x), and with `both` also the total of p alone (.y, the same
+// arithmetic as a walk with q == nullptr).  search == true: stops in the
+// tile, the thread and the logit where the running sum first exceeds `target`
+// and stores that index in *found; when it never does (the target sits
+// within rounding of the slice's end), the last index of positive weight.
+// Both modes do the same arithmetic, so a target below the first mode's total
+// is always crossed.
+constexpr int kGroup = 4;
 template <bool kVec>
-__device__ float walk(const Row& r, int lo, int hi, bool search, float target, float* s_part, int* s_found,
-                      int* found) {
-  float running = 0.0f;
+__device__ float2 walk(const Row& r, int lo, int hi, bool search, bool both, float target, float* s_part, int* s_found,
+                       int* found) {
+  float running = 0.0f, running_p = 0.0f;
   int last_pos = -1;
+  bool done = false;
   const float ninf = __int_as_float(0xff800000);
-  for (int base = lo; base < hi; base += kTile) {
-    const int i = base + 4 * (int)threadIdx.x;
-    const float4 l4 = load4<kVec>(r.l, i, hi, ninf);
-    const float4 q4 = r.q != nullptr ? load4<kVec>(r.q, i, hi, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float w[4] = {weight(r, l4.x, q4.x), weight(r, l4.y, q4.y), weight(r, l4.z, q4.z),
-                        weight(r, l4.w, q4.w)};
-    const float ts = (w[0] + w[1]) + (w[2] + w[3]);
-    float incl, excl;
-    const float tile_total = block_scan(ts, s_part, &incl, &excl);
+  for (int gbase = lo; gbase < hi && !done; gbase += kGroup * kTile) {
+    float4 l4[kGroup], q4[kGroup];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (w[j] > 0.0f) last_pos = i + j;
-    if (search && running + tile_total > target) {
-      // exactly one thread's range (running + excl, running + incl] holds the target
-      if (running + excl <= target && running + incl > target) {
-        float cum = excl;
-        int k = -1, lastj = -1;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (w[j] > 0.0f) lastj = i + j;
-          cum += w[j];
-          if (k < 0 && running + cum > target) k = i + j;
-        }
-        *s_found = k >= 0 ? k : lastj;  // lastj: the 4-term sum rounded past the target
-      }
-      __syncthreads();
-      break;
+    for (int t = 0; t < kGroup; ++t) {
+      const int i = gbase + t * kTile + 4 * (int)threadIdx.x;
+      l4[t] = load4<kVec>(r.l, i, hi, ninf);
+      q4[t] = r.q != nullptr ? load4<kVec>(r.q, i, hi, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    running += tile_total;
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) {
+      const int base = gbase + t * kTile;
+      if (base >= hi) break;  // uniform
+      const int i = base + 4 * (int)threadIdx.x;
+      const float w[4] = {weight(r, l4[t].x, q4[t].x), weight(r, l4[t].y, q4[t].y), weight(r, l4[t].z, q4[t].z),
+                          weight(r, l4[t].w, q4[t].w)};
+      const float ts = (w[0] + w[1]) + (w[2] + w[3]);
+      float incl, excl;
+      const float tile_total = block_scan(ts, s_part, &incl, &excl);
+      if (both) {
+        const Row rp{r.l, nullptr, r.m, r.inv_s};
+        const float wp[4] = {weight(rp, l4[t].x, 0.f), weight(rp, l4[t].y, 0.f), weight(rp, l4[t].z, 0.f),
+                             weight(rp, l4[t].w, 0.f)};
+        float ip, ep;
+        running_p += block_scan((wp[0] + wp[1]) + (wp[2] + wp[3]), s_part, &ip, &ep);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (w[j] > 0.0f) last_pos = i + j;
+      if (search && running + tile_total > target) {
+        // exactly one thread's range (running + excl, running + incl] holds the target
+        if (running + excl <= target && running + incl > target) {
+          float cum = excl;
+          int k = -1, lastj = -1;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (w[j] > 0.0f) lastj = i + j;
+            cum += w[j];
+            if (k < 0 && running + cum > target) k = i + j;
+          }
+          *s_found = k >= 0 ? k : lastj;  // lastj: the 4-term sum rounded past the target
+        }
+        __syncthreads();
+        done = true;
+        break;
+      }
+      running += tile_total;
+    }
   }
   if (search) {
     if (*s_found < 0) atomicMax(s_found, last_pos);
     __syncthreads();
     *found = *s_found;
   }
-  return running;
+  return make_float2(running, both ? running_p : running);
 }
 
 // The lane's accept length a: every CTA evaluates the ratio tests with the
@@ -245,6 +279,7 @@ struct SampleArgs {
   const float* u_sample;
   const float2* stats;  // [B][W]: (M, S) of every row
   float2* totals;       // [B][kMaxSlices]: per slice, (residual weight, p weight) of the drawn row
+  int* counters;        // [B]: CTAs of the lane that have stored their slice totals
   int32_t* accept_len;
   int32_t* out_tokens;
   int32_t* seq_lens;
@@ -256,7 +291,7 @@ struct SampleArgs {
 // Each CTA finds a and stores its slice's total weight of the drawn row (and
 // the total of p_a, for a residual of zero mass).
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_totals_kernel(SampleArgs g) {
+__global__ void __launch_bounds__(kThreads) sample_kernel(SampleArgs g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float s_part[kThreads / 32];
@@ -266,31 +301,23 @@ __global__ void __launch_bounds__(kThreads) sample_totals_kernel(SampleArgs g) {
                              g.status, part == 0, &s_rej);
   Row r = draw_row(g.logits, g.draft_probs, g.window, g.vocab, b, a, g.stats);
   const int lo = part * g.chunk, hi = min(g.vocab, lo + g.chunk);
-  const float res = walk<kVec>(r, lo, hi, false, 0.0f, s_part, nullptr, nullptr);
-  float pt = res;
-  if (r.q != nullptr) {
-    r.q = nullptr;
-    pt = walk<kVec>(r, lo, hi, false, 0.0f, s_part, nullptr, nullptr);
-  }
-  if (threadIdx.x == 0) g.totals[(size_t)b * kMaxSlices + part] = make_float2(res, pt);
-}
-
-// grid (slices, lanes); programmatic dependent of the totals kernel.  Every
-// CTA adds the lane's slice totals in slice order and finds the slice whose
-// running range holds u_sample * Z; that CTA walks its slice again (the same
-// arithmetic) to the crossing.
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_draw_kernel(SampleArgs g) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float s_part[kThreads / 32];
+  const float2 tot = walk<kVec>(r, lo, hi, false, r.q != nullptr, 0.0f, s_part, nullptr, nullptr);
+  __shared__ int s_last, s_found;
   __shared__ float2 s_tot[kMaxSlices];
-  __shared__ int s_rej, s_found;
-  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
-  if (threadIdx.x == 0) s_found = -1;
-  if ((int)threadIdx.x < parts) s_tot[threadIdx.x] = g.totals[(size_t)b * kMaxSlices + threadIdx.x];
-  const int a = accept_count(g.logits, g.draft_probs, g.window, g.vocab, b, g.drafts, g.u_accept, g.stats,
-                             g.status, false, &s_rej);
-  Row r = draw_row(g.logits, g.draft_probs, g.window, g.vocab, b, a, g.stats);
+  if (threadIdx.x == 0) {
+    g.totals[(size_t)b * kMaxSlices + part] = tot;
+    __threadfence();
+    s_last = atomicAdd(&g.counters[b], 1) == (int)gridDim.x - 1;
+    s_found = -1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the lane's last CTA: every slice total is stored; find the slice whose
+  // running range holds u_sample * Z and walk it to the crossing
+  __threadfence();
+  const int parts = gridDim.x;
+  if ((int)threadIdx.x < parts) s_tot[threadIdx.x] = __ldcg(&g.totals[(size_t)b * kMaxSlices + threadIdx.x]);
+  __syncthreads();
   float z = 0.0f;
   for (int p = 0; p < parts; ++p) z += s_tot[p].x;
   const bool use_p = !(z > 0.0f) && r.q != nullptr;  // a residual of zero mass falls back to p_a
@@ -316,19 +343,14 @@ __global__ void __launch_bounds__(kThreads) sample_draw_kernel(SampleArgs g) {
   const bool crossing = owner >= 0;
   if (!crossing) owner = last;
   int32_t* tok = g.out_tokens + (size_t)b * g.window;
-  if (owner < 0) {
-    // no positive weight in the row (only non-finite logits give this)
-    if (part == 0 && threadIdx.x == 0) tok[a] = 0;
-  } else if (part == owner) {
-    const int lo = part * g.chunk, hi = min(g.vocab, lo + g.chunk);
-    int k = -1;
-    walk<kVec>(r, lo, hi, true, crossing ? target - before : __int_as_float(0x7f800000), s_part, &s_found, &k);
-    if (threadIdx.x == 0) tok[a] = k;
+  int k = 0;  // no positive weight in the row (only non-finite logits give this)
+  if (owner >= 0) {
+    const int olo = owner * g.chunk, ohi = min(g.vocab, olo + g.chunk);
+    walk<kVec>(r, olo, ohi, true, false, crossing ? target - before : __int_as_float(0x7f800000), s_part, &s_found, &k);
   }
-  if (part == 0 && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     const int d = g.window - 1;
-    for (int i = 0; i < g.window; ++i)
-      if (i != a) tok[i] = i < a ? g.drafts[(size_t)b * d + i] : -1;
+    for (int i = 0; i < g.window; ++i) tok[i] = i == a ? k : (i < a ? g.drafts[(size_t)b * d + i] : -1);
     g.accept_len[b] = a;
     if (g.seq_lens != nullptr) g.seq_lens[b] += 1 + a;
   }
@@ -347,11 +369,12 @@ namespace {
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 }  // namespace
 
-// per-row statistics [B][W], then per-slice totals of the drawn rows [B][kMaxSlices]
+// per-row statistics [B][W], per-slice totals of the drawn rows [B][kMaxSlices],
+// then the draw's per-lane counters [B]
 extern "C" size_t spec_accept_sampled_workspace_size(int num_lanes, int window) {
   if (num_lanes <= 0 || window <= 0) return 0;
   return align256((size_t)num_lanes * window * sizeof(float2)) +
-         align256((size_t)num_lanes * kMaxSlices * sizeof(float2));
+         align256((size_t)num_lanes * kMaxSlices * sizeof(float2)) + align256((size_t)num_lanes * sizeof(int));
 }
 
 extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs, int num_lanes, int window,
@@ -374,6 +397,9 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
     return SDVA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float2* stats = static_cast<float2*>(workspace);
+  int* counters = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                         align256((size_t)num_lanes * window * sizeof(float2)) +
+                                         align256((size_t)num_lanes * kMaxSlices * sizeof(float2)));
   const bool vec = vectorizable(logits, vocab) && (window == 1 || vectorizable(draft_probs, vocab));
   {
     // CTAs per row: enough to cover every SM about four times, at most one portable cluster
@@ -392,7 +418,8 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const auto kernel = vec ? row_stats_kernel<true> : row_stats_kernel<false>;
-    if (cudaLaunchKernelEx(&cfg, kernel, logits, vocab, chunk, stats) != cudaSuccess) return SDVA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, logits, vocab, chunk, stats, counters, num_lanes) != cudaSuccess)
+      return SDVA_ERR_CUDA;
   }
   SampleArgs g;
   g.logits = logits;
@@ -403,6 +430,7 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
   g.stats = stats;
   g.totals = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
                                        align256((size_t)num_lanes * window * sizeof(float2)));
+  g.counters = counters;
   g.accept_len = accept_len;
   g.out_tokens = out_tokens;
   g.seq_lens = seq_lens_inout;
@@ -411,7 +439,7 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
   g.vocab = vocab;
   const int slices = min(kMaxSlices, max(1, (vocab + kSampleSlice - 1) / kSampleSlice));
   g.chunk = (((vocab + slices - 1) / slices) + 3) & ~3;
-  for (int k = 0; k < 2; ++k) {
+  {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(slices, (unsigned)num_lanes, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -421,8 +449,7 @@ extern "C" int spec_accept_sampled(const float* logits, const float* draft_probs
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const auto kernel = k == 0 ? (vec ? sample_totals_kernel<true> : sample_totals_kernel<false>)
-                               : (vec ? sample_draw_kernel<true> : sample_draw_kernel<false>);
+    const auto kernel = vec ? sample_kernel<true> : sample_kernel<false>;
     if (cudaLaunchKernelEx(&cfg, kernel, g) != cudaSuccess) return SDVA_ERR_CUDA;
   }
   return SDVA_OK;
