@@ -319,34 +319,108 @@ def oracle_steps(spec, step, cache, lanes, threads, n_steps=None, budget_s=None)
     return total / max(1, len(times)), (work / full) / total, len(times)
 
 
+REFERENCE_BUDGET_S = 120.0  # host time the reference arm's warm-up and timed steps aim at together
+
+
 def run_reference(args):
-    """The reference arm: the CPU oracle on the host cores.  Each timed step
-    is one lane of the workload (its window append, all window rows of its
-    attention in fp64, its acceptance), cycling over the lanes; `value`
-    counts the work done in whole-workload steps per second."""
+    """The reference arm: the CPU oracle on the host cores, sized by a
+    calibration so that the W + K steps take about REFERENCE_BUDGET_S
+    together, whatever W and K are.  When a step's share allows at least one
+    wave of rows over all threads, a step is a run of consecutive attention
+    rows of the workload (lane by lane, window position by position, head by
+    head, cycling), each lane's window append and acceptance done in the step
+    that reaches its first and last row; otherwise a step is one row over as
+    many of its keys as its share allows, on one thread.  `value` counts the
+    keys attended in whole-workload steps per second."""
+    import oracle
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     spec = all_workload_specs()[args.workload]
     step = synth.make_step(spec)
-    B = len(step.seq_lens)
+    B, W, Hq = step.q.shape[:3]
     lanes = list(range(B))
     cache = oracle_setup(spec, step, lanes)
     threads = os.cpu_count() or 1
-    # warm-up steps on the shortest lane (the oracle is compiled C: nothing to warm but caches)
-    oracle_steps(spec, step, cache, [int(np.argmin(step.seq_lens))], threads, n_steps=args.warmup)
-    sec, value, n = oracle_steps(spec, step, cache, lanes, threads, n_steps=args.steps)
+    rows_all = [(b, i, h) for b in lanes for i in range(W) for h in range(Hq)]
+    full = sum(lane_work(spec, L) for L in step.seq_lens)
+    per_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    # calibration on the median lane: one wave of `threads` rows in parallel
+    bm = int(np.argsort(step.seq_lens)[len(lanes) // 2])
+    wave = [(bm, i, h) for i in range(W) for h in range(Hq)][:max(1, min(threads, W * Hq))]
+    t0 = time.perf_counter()
+    oracle.verify_attn(cache, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=wave, threads=threads)
+    t_wave = time.perf_counter() - t0
+    row_mode = per_step >= t_wave
+    if row_mode:
+        # whole rows: a multiple of the thread count, at most one lane's window
+        rows_per_step = int(min(W * Hq, len(wave) * max(1, int(per_step // t_wave))))
+        cores = min(threads, rows_per_step)
+    else:
+        # a step shorter than one wave of rows: one row over the first n_keys of its keys, on one thread
+        L0 = int(step.seq_lens[bm])
+        t0 = time.perf_counter()
+        oracle.decode_row(cache, step.q[bm, 0, 0], 0, step.page_table[bm], L0 + 1, SM_SCALE)
+        sec_per_key = (time.perf_counter() - t0) / (L0 + 1)
+        rows_per_step = 1
+        cores = 1
+    pos = 0
+
+    def one_step():
+        nonlocal pos
+        if not row_mode:
+            b, i, h = rows_all[pos % len(rows_all)]
+            pos = (pos + 1) % len(rows_all)
+            n_keys = int(max(1, min(int(step.seq_lens[b]) + i + 1, per_step / max(sec_per_key, 1e-12))))
+            t1 = time.perf_counter()
+            oracle.decode_row(cache, step.q[b, i, h], h // (Hq // spec.num_kv_heads), step.page_table[b], n_keys,
+                              SM_SCALE)
+            return time.perf_counter() - t1, n_keys
+        rows = [rows_all[(pos + k) % len(rows_all)] for k in range(rows_per_step)]
+        pos = (pos + rows_per_step) % len(rows_all)
+        t1 = time.perf_counter()
+        for (b, i, h) in rows:
+            if i == 0 and h == 0:  # the lane's append precedes its attention
+                sel = slice(b, b + 1)
+                oracle.append(cache, step.k_win[sel], step.v_win[sel], step.page_table[sel], step.seq_lens[sel])
+        oracle.verify_attn(cache, step.q, step.page_table, step.seq_lens, SM_SCALE, rows=rows, threads=threads)
+        for (b, i, h) in rows:
+            if i == W - 1 and h == Hq - 1 and step.logits is not None:  # the lane's acceptance
+                sel = slice(b, b + 1)
+                oracle.spec_accept(step.logits[sel], step.drafts[sel], step.seq_lens[sel])
+        dt = time.perf_counter() - t1
+        return dt, sum(int(step.seq_lens[b]) + i + 1 for (b, i, h) in rows)
+
+    for _ in range(args.warmup):
+        one_step()
+    times, work = [], 0
+    for _ in range(args.steps):
+        dt, wk = one_step()
+        times.append(dt)
+        work += wk
+    total = float(np.sum(times))
+    value = (work / full) / total if total > 0 else 0.0
     model = cpu_model()
-    sample = (f"each timed step: one lane of the {B}-lane workload, cycling over the lanes -- its window append, "
-              f"all {spec.window} x {spec.num_q_heads} attention rows over its whole context in fp64 "
-              f"({threads} threads), its acceptance; value = whole-workload steps/s of the work done")
+    if row_mode:
+        unit = f"{rows_per_step} attention rows per timed step"
+        sample = (f"each step: {rows_per_step} consecutive attention rows of the {B}-lane workload (of "
+                  f"{len(rows_all)}), cycling over lanes, window positions and heads, over each row's whole "
+                  f"context in fp64 ({cores} threads), a lane's window append and acceptance in the step that "
+                  f"reaches its first and last row")
+    else:
+        unit = "one attention row over a bounded number of its keys per timed step"
+        sample = (f"each step: one attention row of the {B}-lane workload, cycling over lanes, window positions "
+                  f"and heads, over its first keys (as many as the step's share of the budget allows), fp64 on "
+                  f"one thread")
+    sample += (f"; sized so that {args.warmup} + {args.steps} steps take about {REFERENCE_BUDGET_S:.0f} s; "
+               f"value = whole-workload steps/s of the keys attended")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / max(1, args.steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": bench_config(spec, step.seq_lens, world),
-        "step_unit": "one lane per timed step (see cpu_baseline.sample)",
-        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle", "cpu": model,
+        "step_unit": f"{unit} (see cpu_baseline.sample)",
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle", "cpu": model,
                          "sample": sample},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
