@@ -65,6 +65,34 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
     assert capsys.readouterr().out == ""
 
 
+@pytest.mark.parametrize("steps,budget", [(3, 30.0), (400, 0.5)], ids=["row-mode", "key-mode"])
+def test_reference_arm_line_and_bounded_time(monkeypatch, capsys, steps, budget):
+    """Rank 0 prints one contract line with impl reference; every step is
+    sized from the run's budget (whole rows when a step can afford a wave of
+    them, else one row over a bounded number of keys), so K x ms_per_step is
+    the measured time of the timed steps and the run stays near the budget."""
+    import json
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", budget)
+    args = bench.argparse.Namespace(workload="tiny", steps=steps, warmup=3, gpus=1)
+    t0 = time.perf_counter()
+    assert bench.run_reference(args) == 0
+    wall = time.perf_counter() - t0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == steps and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert steps * line["ms_per_step"] / 1e3 <= wall
+    if steps == 3:
+        assert "attention rows per timed step" in line["step_unit"]
+    else:
+        assert "bounded number of its keys" in line["step_unit"] and line["cpu_baseline"]["cores"] == 1
+
+
 def test_verify_algorithmic_bytes_counts_the_cache_layout():
     """The roofline's bytes, counted from the oracle's cache arrays: every
     visible key's K and V codes and the scales that cover it, Q in, O out,
