@@ -8,7 +8,8 @@
 //
 // Kernel 1 (argmax): one thread-block cluster of up to 8 CTAs per logits
 // row; each CTA scans a contiguous slice of the row with 16-byte streaming
-// loads, four in flight per thread (32 registers, so eight 256-thread CTAs fit
+// loads, four in flight per thread and the next four requested into L2
+// (32 registers, so eight 256-thread CTAs fit
 // on an SM and the grid of the multi-row case is a single wave), keeps its
 // best with one greater-than test per element (exact, since a thread meets
 // its elements in index order; a thread that met nothing above -inf rescans
@@ -116,6 +117,10 @@ __device__ __forceinline__ void scan_vec(const float4* x4, int k, int kend, int 
     float4 v[kLoads];
 #pragma unroll
     for (int u = 0; u < kLoads; ++u) v[u] = __ldcs(x4 + k + u * step);
+    // the next group's lines requested into L2 while this one is in flight
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u)
+      if (k + (kLoads + u) * step < kend) asm volatile("prefetch.global.L2 [%0];" ::"l"(x4 + k + (kLoads + u) * step));
 #pragma unroll
     for (int u = 0; u < kLoads; ++u) take4_as<kExact>(v[u], 4 * (k + u * step), bv, bi);
   }
