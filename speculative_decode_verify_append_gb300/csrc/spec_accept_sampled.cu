@@ -12,7 +12,8 @@
 //
 // Kernel 1 (row statistics): one cluster of up to 8 CTAs per logits row; each
 // CTA reduces its slice to (running max, sum of exp) with 16-byte streaming
-// loads, four in flight per thread, the cluster combines the slices in rank
+// loads, four in flight per thread and the next four requested into L2, the
+// cluster combines the slices in rank
 // order through distributed shared memory, and rank 0 stores (M, S) of the
 // row in the workspace.  All rows are reduced at once over the whole GPU (the
 // acceptance needs S of every row up to the first rejection).
@@ -95,6 +96,10 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* logits
     float4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = load4<kVec>(x, i + 4 * kThreads * u, hi, ninf);
+    // the next four requested into L2 while these are in flight
+#pragma unroll
+    for (int u = 4; u < 8; ++u)
+      if (i + 4 * kThreads * u + 3 < hi) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + i + 4 * kThreads * u));
 #pragma unroll
     for (int u = 0; u < 4; ++u) st = add4(st, v[u]);
   }
