@@ -546,6 +546,142 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
   const uint32_t v16 = base + SM::kOffV16;
   const uint32_t k16 = base + SM::kOffK16;
   const uint32_t qsm = base + SM::kOffQ;
+  // The V (and INT K) widening of every page, run by converter thread u
+  // (0 .. 32 * kConvWarps - 1) of the warps that take the converter role.
+  auto convert = [&](const int u) {
+    // ------------------------------------------------------------------
+    // converters: page g's V codes (TMA tile, 128-byte swizzle, row = key)
+    // -> fp16 in V16 slot g % kV16Stages: dims 0-63 and 64-127 as two
+    // 64-row x 128-byte regions, each with the 128-byte swizzle (16-byte
+    // chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  E4M3 -> fp16 is
+    // exact.  Converter thread u handles the items u, u + kCT, ... of a page
+    // (kCT converter threads; the row and chunk of an item follow below).
+    // ------------------------------------------------------------------
+    constexpr int kCT = 32 * SM::kConvWarps;  // converter threads
+    // Shared memory serves a warp's 16-byte accesses a quarter-warp (8
+    // lanes) at a time, and the two 8 KB halves of an fp16 tile share banks:
+    // each quarter-warp takes two rows whose stores land in 8 distinct
+    // 16-byte bank groups (as do its loads).  Lane l of a warp covering rows
+    // r0 .. : row offset rof, 16-dim chunk c8 (FP8, INT8) or group g4 (INT4).
+    const int q8 = lane >> 3, rr = (lane >> 2) & 1;
+    const int c8 = (lane & 3) + 4 * (rr ^ (q8 & 1));                        // rows r0 + rof, 4 per warp
+    const int rof8 = 2 * (q8 >> 1) + rr;
+    const int hb = (lane >> 2) & 1, r4 = (lane >> 1) & 1;                   // INT4: 8 rows per warp
+    const int g4 = (lane & 1) + 2 * (hb ^ (q8 & 1));
+    const int rof4 = 4 * (q8 >> 1) + 2 * hb + r4;
+    bool ok = true;
+    for (long long h = 0; h < n_local && ok; ++h) {
+      const int s = (int)((uint32_t)h % (uint32_t)kNS), t = (int)((uint32_t)h % (uint32_t)kV16Stages);
+      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)(((uint32_t)h / (uint32_t)kNS) & 1), abort_flag, a.wait_limit))) break;
+      if (h >= kV16Stages &&
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
+        break;
+      if (kDeq && h >= kV16Stages &&
+          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
+        break;
+      const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
+      uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
+      if constexpr (SM::kInt8) {
+        // INT8: K and V, 64 rows x 8 chunks of 16 dims each; chunk (tk, r, c)
+        // -> 2 chunks of 8 dims in the swizzled fp16 layout (K: the K-major
+        // operand of the QK MMA; V: the MN-major operand of the PV MMA)
+        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
+#pragma unroll 4
+        for (int q = 0; q < 1024 / kCT; ++q) {
+          const int item = u + kCT * q;  // 1024 chunks per page, 32 per warp: 4 rows x 8 chunks
+          const int tk = item >> 9, r = 4 * ((item & 511) >> 5) + rof8, c = c8;
+          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 128 + c * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes +
+                                                                 r * 4 + (c >> 2) * 2);
+          uint32_t h16[8];
+          int8x16_to_f16(codes, sc, h16);
+          // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
+          uint8_t* reg = (tk ? dst : kdst) + (c >> 2) * 8192 + r * 128;
+          const int c0 = 2 * (c & 3);
+          *reinterpret_cast<uint4*>(reg + ((c0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+          *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+        }
+      } else if constexpr (kDeq) {
+        // INT4: K and V, 64 rows x 4 groups of 32 dims each; group (tk, r, gi)
+        // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
+        // it is the K-major operand of the QK MMA)
+        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
+        constexpr int kQ = 512 / kCT;
+        uint4 codes4[kQ];
+        uint32_t sc4[kQ];
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const int item = u + kCT * q;
+          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
+          codes4[q] = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
+          sc4[q] = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
+        }
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const int item = u + kCT * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
+          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
+          uint4 ch[4];
+          int4_group_to_f16(codes4[q], sc4[q], ch);
+          // dims 32gi .. 32gi + 31 -> region gi >> 1, 8-dim chunks 4 (gi & 1) .. + 3
+          uint8_t* reg = (tk ? dst : kdst) + (gi >> 1) * 8192 + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(reg + (((4 * (gi & 1) + k) ^ (r & 7)) << 4)) = ch[k];
+        }
+      } else {
+        const uint8_t* src = stage + kTileBytes;
+        // FP8 row: row r is widened as code * (s_r / s_max) (zero past the
+        // page's written rows); the softmax folds s_max into its shift
+        const float* rs = reinterpret_cast<const float*>(base_ptr + SM::kOffRowSc + s * kRowScaleBytes);
+        int nv = 0;
+        float inv_max = 0.0f;
+        if constexpr (kRow) {
+          nv = ctl->nv[s];
+          const float vmax = row_vscale_max(rs, nv, lane);
+          inv_max = vmax > 0.0f ? __fdividef(1.0f, vmax) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+        const int item = u + 128 * q;  // 512 chunks per page, 32 per warp: 4 rows x 8 chunks
+        const int r = 4 * (item >> 5) + rof8, c = c8;  // key row, 16-dim chunk
+        const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+        const uint32_t b[4] = {w.x, w.y, w.z, w.w};
+        uint32_t h16[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          h16[2 * k] = f16x2_from_e4m3x2(b[k] & 0xFFFFu);
+          h16[2 * k + 1] = f16x2_from_e4m3x2(b[k] >> 16);
+        }
+        if constexpr (kRow) {
+          const __half2 f2 = __float2half2_rn(r < nv ? rs[64 + r] * inv_max : 0.0f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h16[k]), f2);
+            h16[k] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+        }
+        // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
+        uint8_t* reg = dst + (c >> 2) * 8192 + r * 128;
+        const int c0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(reg + (((c0) ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+        *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+        }
+      }
+      // generic-proxy writes -> visible to the tensor core
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->v16_full[t]));
+        if (kDeq) mbar_arrive(smem_u32(&ctl->k16_full[t]));
+        mbar_arrive(smem_u32(&ctl->empty[s]));
+      }
+    }
+    if (!ok) fail(ctl, a.status);
+  };
+  // FP8 page scales with at most 64 rows per kv head: the softmax warps that own
+  // no rows (sub-partitions 2-3) convert, so the converters' issue load leaves
+  // the sub-partitions that run the row warps; warps 12-15 then stand aside
+  const bool conv_on_idle = KVT == SDVA_KV_FP8_E4M3 && a.R <= 64;
   // Each warpgroup changes its register budget as a whole, before its warps
   // take their roles.
   if (warp >= 8) {
@@ -819,135 +955,7 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       }
     }
   } else if (warp >= kConvWarp) {
-    // ------------------------------------------------------------------
-    // converters: page g's V codes (TMA tile, 128-byte swizzle, row = key)
-    // -> fp16 in V16 slot g % kV16Stages: dims 0-63 and 64-127 as two
-    // 64-row x 128-byte regions, each with the 128-byte swizzle (16-byte
-    // chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4)).  E4M3 -> fp16 is
-    // exact.  Converter thread u handles the items u, u + kCT, ... of a page
-    // (kCT converter threads; the row and chunk of an item follow below).
-    // ------------------------------------------------------------------
-    const int u = threadIdx.x - kConvWarp * 32;
-    constexpr int kCT = 32 * SM::kConvWarps;  // converter threads
-    // Shared memory serves a warp's 16-byte accesses a quarter-warp (8
-    // lanes) at a time, and the two 8 KB halves of an fp16 tile share banks:
-    // each quarter-warp takes two rows whose stores land in 8 distinct
-    // 16-byte bank groups (as do its loads).  Lane l of a warp covering rows
-    // r0 .. : row offset rof, 16-dim chunk c8 (FP8, INT8) or group g4 (INT4).
-    const int q8 = lane >> 3, rr = (lane >> 2) & 1;
-    const int c8 = (lane & 3) + 4 * (rr ^ (q8 & 1));                        // rows r0 + rof, 4 per warp
-    const int rof8 = 2 * (q8 >> 1) + rr;
-    const int hb = (lane >> 2) & 1, r4 = (lane >> 1) & 1;                   // INT4: 8 rows per warp
-    const int g4 = (lane & 1) + 2 * (hb ^ (q8 & 1));
-    const int rof4 = 4 * (q8 >> 1) + 2 * hb + r4;
-    bool ok = true;
-    for (long long h = 0; h < n_local && ok; ++h) {
-      const int s = (int)((uint32_t)h % (uint32_t)kNS), t = (int)((uint32_t)h % (uint32_t)kV16Stages);
-      if (!(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->full[s]), (uint32_t)(((uint32_t)h / (uint32_t)kNS) & 1), abort_flag, a.wait_limit))) break;
-      if (h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->v16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
-        break;
-      if (kDeq && h >= kV16Stages &&
-          !(ok = mbar_wait<kSpinWait>(smem_u32(&ctl->k16_empty[t]), (uint32_t)(((uint32_t)h / (uint32_t)kV16Stages - 1) & 1), abort_flag, a.wait_limit)))
-        break;
-      const uint8_t* stage = base_ptr + SM::kOffStages + s * kStageBytes;
-      uint8_t* dst = base_ptr + SM::kOffV16 + t * kV16Bytes;
-      if constexpr (SM::kInt8) {
-        // INT8: K and V, 64 rows x 8 chunks of 16 dims each; chunk (tk, r, c)
-        // -> 2 chunks of 8 dims in the swizzled fp16 layout (K: the K-major
-        // operand of the QK MMA; V: the MN-major operand of the PV MMA)
-        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
-#pragma unroll 4
-        for (int q = 0; q < 1024 / kCT; ++q) {
-          const int item = u + kCT * q;  // 1024 chunks per page, 32 per warp: 4 rows x 8 chunks
-          const int tk = item >> 9, r = 4 * ((item & 511) >> 5) + rof8, c = c8;
-          const uint4 codes = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 128 + c * 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes +
-                                                                 r * 4 + (c >> 2) * 2);
-          uint32_t h16[8];
-          int8x16_to_f16(codes, sc, h16);
-          // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
-          uint8_t* reg = (tk ? dst : kdst) + (c >> 2) * 8192 + r * 128;
-          const int c0 = 2 * (c & 3);
-          *reinterpret_cast<uint4*>(reg + ((c0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-          *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-        }
-      } else if constexpr (kDeq) {
-        // INT4: K and V, 64 rows x 4 groups of 32 dims each; group (tk, r, gi)
-        // -> 4 chunks of 8 dims in the same swizzled fp16 layout as V (for K
-        // it is the K-major operand of the QK MMA)
-        uint8_t* kdst = base_ptr + SM::kOffK16 + t * kV16Bytes;
-        constexpr int kQ = 512 / kCT;
-        uint4 codes4[kQ];
-        uint32_t sc4[kQ];
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-          const int item = u + kCT * q;
-          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
-          codes4[q] = *reinterpret_cast<const uint4*>(stage + tk * SM::kCodeBytes + r * 64 + gi * 16);
-          sc4[q] = *reinterpret_cast<const uint16_t*>(stage + 2 * SM::kCodeBytes + tk * SM::kScaleBytes + r * 8 + gi * 2);
-        }
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-          const int item = u + kCT * q;  // 512 groups per page, 32 per warp: 8 rows x 4 groups
-          const int tk = item >> 8, r = 8 * ((item & 255) >> 5) + rof4, gi = g4;
-          uint4 ch[4];
-          int4_group_to_f16(codes4[q], sc4[q], ch);
-          // dims 32gi .. 32gi + 31 -> region gi >> 1, 8-dim chunks 4 (gi & 1) .. + 3
-          uint8_t* reg = (tk ? dst : kdst) + (gi >> 1) * 8192 + r * 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(reg + (((4 * (gi & 1) + k) ^ (r & 7)) << 4)) = ch[k];
-        }
-      } else {
-        const uint8_t* src = stage + kTileBytes;
-        // FP8 row: row r is widened as code * (s_r / s_max) (zero past the
-        // page's written rows); the softmax folds s_max into its shift
-        const float* rs = reinterpret_cast<const float*>(base_ptr + SM::kOffRowSc + s * kRowScaleBytes);
-        int nv = 0;
-        float inv_max = 0.0f;
-        if constexpr (kRow) {
-          nv = ctl->nv[s];
-          const float vmax = row_vscale_max(rs, nv, lane);
-          inv_max = vmax > 0.0f ? __fdividef(1.0f, vmax) : 0.0f;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-        const int item = u + 128 * q;  // 512 chunks per page, 32 per warp: 4 rows x 8 chunks
-        const int r = 4 * (item >> 5) + rof8, c = c8;  // key row, 16-dim chunk
-        const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
-        const uint32_t b[4] = {w.x, w.y, w.z, w.w};
-        uint32_t h16[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          h16[2 * k] = f16x2_from_e4m3x2(b[k] & 0xFFFFu);
-          h16[2 * k + 1] = f16x2_from_e4m3x2(b[k] >> 16);
-        }
-        if constexpr (kRow) {
-          const __half2 f2 = __float2half2_rn(r < nv ? rs[64 + r] * inv_max : 0.0f);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h16[k]), f2);
-            h16[k] = *reinterpret_cast<const uint32_t*>(&v);
-          }
-        }
-        // dims 16c .. 16c + 15 -> region c >> 2, 8-dim chunks 2 (c & 3) and 2 (c & 3) + 1
-        uint8_t* reg = dst + (c >> 2) * 8192 + r * 128;
-        const int c0 = 2 * (c & 3);
-        *reinterpret_cast<uint4*>(reg + (((c0) ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-        *reinterpret_cast<uint4*>(reg + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-        }
-      }
-      // generic-proxy writes -> visible to the tensor core
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctl->v16_full[t]));
-        if (kDeq) mbar_arrive(smem_u32(&ctl->k16_full[t]));
-        mbar_arrive(smem_u32(&ctl->empty[s]));
-      }
-    }
-    if (!ok) fail(ctl, a.status);
+    if (!conv_on_idle) convert(threadIdx.x - kConvWarp * 32);
   }
   } else {
     regs_increase<SM::kConvWarps == 8 ? kRegsSoftmax20 : kRegsSoftmax>();
@@ -955,6 +963,10 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
     // softmax warpgroups: wg 0 = warps 0-3 (even positions), wg 1 = warps
     // 4-7 (odd positions); thread = query row = TMEM lane
     // ------------------------------------------------------------------
+  if ((warp & 3) * 32 >= a.R) {
+    // a softmax warp that owns no query rows
+    if (conv_on_idle && (warp & 3) >= 2) convert(((warp >> 2) * 2 + (warp & 3) - 2) * 32 + lane);
+  } else {
     const int wg = warp >> 2;
     const int row = threadIdx.x & 127;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -1193,13 +1205,13 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
         ctl->m1[row] = (had_page && warp_active) ? m : -INFINITY;
         ctl->l1[row] = (had_page && warp_active) ? l : 0.0f;
         if (row == 0) ctl->bad1 = seg_bad;
-        named_arrive(kBarWg1Done, 256);
-        named_sync(kBarWg0Done, 256);  // warpgroup 0 has read this warpgroup's O
+        named_arrive(kBarWg1Done, 2 * row_threads);
+        named_sync(kBarWg0Done, 2 * row_threads);  // warpgroup 0 has read this warpgroup's O
         fence_after_sync();
         if (ctl->stop) break;
         continue;
       }
-      named_sync(kBarWg1Done, 256);
+      named_sync(kBarWg1Done, 2 * row_threads);
       fence_after_sync();
       const bool stop = !ok || *abort_flag;
       const bool had0 = seg_len > 1 || (g_first & 1) == 0;  // warpgroup 0 owned a page of this segment
@@ -1275,9 +1287,10 @@ __global__ void __launch_bounds__(Smem<KVT>::kThreads, 1) verify_split_tc_kernel
       }
       if (threadIdx.x == 0) ctl->stop = stop ? 1 : 0;
       fence_before_sync();
-      named_arrive(kBarWg0Done, 256);
+      named_arrive(kBarWg0Done, 2 * row_threads);
       if (stop) break;
     }
+  }
   }
 
   fence_before_sync();
