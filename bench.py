@@ -60,9 +60,9 @@ DEFAULT_WORKLOAD = "multi_lane"
 # from an ncu capture of the kernels built from sources with this SHA-256
 # (verify_attn_tc.cu, tc_primitives.cuh, verify_attn.cu, in that order, comments stripped);
 # reported as null once the sources differ (the counters are then stale).
-NCU_TRAFFIC = {"sources_sha256": "266255b2b84e5ce0a5d97998359ecbed418951c7ce3859058e5f67fea4f96e0f",
-               "bytes": {"multi_lane": 314619392, "long_context": 249027328, "int4_12slot": 337949696,
-                         "multi_lane_int8": 324121856, "multi_lane_fp8row": 323734784}}
+NCU_TRAFFIC = {"sources_sha256": "44309ab667511223cc8f80338fd680afc3acd8be96ad613058a6664407bfaf02",
+               "bytes": {"multi_lane": 314707456, "long_context": 249022464, "int4_12slot": 338031360,
+                         "multi_lane_int8": 324021760, "multi_lane_fp8row": 323727872}}
 TRAFFIC_SOURCES = ("verify_attn_tc.cu", "tc_primitives.cuh", "verify_attn.cu")
 
 
