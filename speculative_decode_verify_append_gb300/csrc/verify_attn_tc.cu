@@ -21,7 +21,9 @@
 //     128-byte swizzle) into a ring of shared-memory stages, and stages the
 //     page's scale terms (FP8 formats; the row scales by bulk copies); the
 //     INT4 and INT8 codes and scales arrive by 1-D bulk copies.
-//   * Warps 12-15, 12-19 for INT8 (converters): widen each page's V codes to fp16 (exact for
+//   * Warps 12-15, 12-19 for INT8 (converters; for FP8 page scales at R <= 64
+//     the softmax warps without rows on sub-partitions 2-3 take this role
+//     instead): widen each page's V codes to fp16 (exact for
 //     E4M3; FP8 row: times s_j / s_max; INT4 and INT8: times the group scale)
 //     into a second ring, laid out as the MN-major operand of the PV MMA; for
 //     INT4 and INT8 also the K codes, into a third ring.
