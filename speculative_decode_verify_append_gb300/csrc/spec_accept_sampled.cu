@@ -294,7 +294,8 @@ struct SampleArgs {
 
 // grid (slices, lanes); programmatic dependent of the statistics kernel.
 // Each CTA finds a and stores its slice's total weight of the drawn row (and
-// the total of p_a, for a residual of zero mass).
+// the total of p_a, for a residual of zero mass); the lane's last CTA to count
+// itself draws the token, writes the tokens and a, and commits seq_lens.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) sample_kernel(SampleArgs g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
